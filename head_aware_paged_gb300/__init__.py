@@ -1,0 +1,294 @@
+"""head_aware_paged_gb300 -- head-aware paged KV cache and mask-free attention
+for one GB300 GPU.
+
+Thin Python binding over libsegpaged.so (include/segpaged.h).  The functions
+below carry the C-ABI names and only marshal arguments: torch tensors are
+passed as device pointers together with torch's current CUDA stream; torch
+supplies device memory and streams, the library's kernels do all the work.
+
+    cache = SegPagedCache(cfg)                        # allocates pool/meta/ws
+    cache.set_policy(seq, policies)                   # [layers][kv_heads]
+    out, lse = cache.prefill(layer, [seq], [0, T], q, k, v)
+    cache.append_kv(layer, [seq], [0, T], k, v)
+    cache.append_kv(layer, [seq], [0, 1], k1, v1)
+    out, lse = cache.decode(layer, [seq], q1)
+"""
+from __future__ import annotations
+
+import ctypes
+from ctypes import byref, c_int32, c_int64, c_size_t, c_void_p
+from dataclasses import dataclass
+from typing import List, Optional, Sequence
+
+import torch
+
+from ._lib import (EXPORTS, GLOBAL, LOCAL, RETRIEVAL, SegPagedError, SpConfig, SpHeadPolicy,
+                   check, i32_array, i64_array, load)
+
+__all__ = ["Config", "Policy", "SegPagedCache", "SegPagedError", "GLOBAL", "LOCAL",
+           "RETRIEVAL", "load", "EXPORTS"] + list(EXPORTS)
+
+
+@dataclass
+class Config:
+    num_layers: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    page_size: int
+    max_seqs: int
+    max_seq_len: int
+    num_pages: int
+    max_idx_per_seq: int = 0
+    max_tokens: int = 8192
+    max_batch: int = 1
+
+    def to_c(self) -> SpConfig:
+        return SpConfig(self.num_layers, self.num_q_heads, self.num_kv_heads, self.head_dim,
+                        self.page_size, self.max_seqs, self.max_seq_len, self.num_pages,
+                        self.max_idx_per_seq, self.max_tokens, self.max_batch)
+
+
+@dataclass
+class Policy:
+    kind: int
+    sink: int = 0
+    window: int = 0
+    idx: Optional[Sequence[int]] = None
+
+
+def _stream(stream=None) -> c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return c_void_p(int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t: Optional[torch.Tensor]) -> c_void_p:
+    return c_void_p(0 if t is None else t.data_ptr())
+
+
+# ---------------------------------------------------------------- C-ABI names
+
+def sp_required_bytes(cfg: Config):
+    lib = load()
+    a, b, c = c_size_t(), c_size_t(), c_size_t()
+    check(lib.sp_required_bytes(byref(cfg.to_c()), byref(a), byref(b), byref(c)))
+    return a.value, b.value, c.value
+
+
+def sp_cache_create(cfg: Config, pool: torch.Tensor, meta: torch.Tensor, ws: torch.Tensor):
+    lib = load()
+    h = c_void_p()
+    check(lib.sp_cache_create(byref(cfg.to_c()), _ptr(pool), _ptr(meta), _ptr(ws), byref(h)))
+    return h
+
+
+def sp_cache_destroy(handle) -> None:
+    check(load().sp_cache_destroy(handle))
+
+
+def _policy_array(policies: Sequence[Policy]):
+    arr = (SpHeadPolicy * len(policies))()
+    keep = []
+    for n, p in enumerate(policies):
+        idx = list(p.idx) if p.idx is not None else []
+        buf = i32_array(idx)
+        keep.append(buf)
+        arr[n] = SpHeadPolicy(p.kind, p.sink, p.window, len(idx),
+                              ctypes.cast(buf, ctypes.POINTER(c_int32)))
+    return arr, keep
+
+
+def sp_set_policy(handle, seq: int, policies: Sequence[Policy], stream=None) -> None:
+    arr, keep = _policy_array(policies)
+    check(load().sp_set_policy(handle, seq, arr, _stream(stream)))
+    del keep
+
+
+def sp_build_cache(handle, seq: int, layer: int, k: torch.Tensor, v: torch.Tensor,
+                   n_tokens: int, row_stride: int, stream=None) -> None:
+    check(load().sp_build_cache(handle, seq, layer, _ptr(k), _ptr(v), n_tokens, row_stride,
+                                _stream(stream)))
+
+
+def sp_append_kv(handle, layer: int, seq_ids: Sequence[int], cu_new: Sequence[int],
+                 k: torch.Tensor, v: torch.Tensor, stream=None) -> None:
+    check(load().sp_append_kv(handle, layer, i32_array(seq_ids), len(seq_ids),
+                              i32_array(cu_new), _ptr(k), _ptr(v), _stream(stream)))
+
+
+def sp_attention_prefill(handle, layer: int, seq_ids: Sequence[int], cu_q: Sequence[int],
+                         q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor,
+                         lse: Optional[torch.Tensor] = None, stream=None) -> None:
+    check(load().sp_attention_prefill(handle, layer, i32_array(seq_ids), len(seq_ids),
+                                      i32_array(cu_q), _ptr(q), _ptr(k), _ptr(v), _ptr(out),
+                                      _ptr(lse), _stream(stream)))
+
+
+def sp_attention_decode(handle, layer: int, seq_ids: Sequence[int], q: torch.Tensor,
+                        out: torch.Tensor, lse: Optional[torch.Tensor] = None,
+                        stream=None) -> None:
+    check(load().sp_attention_decode(handle, layer, i32_array(seq_ids), len(seq_ids), _ptr(q),
+                                     _ptr(out), _ptr(lse), _stream(stream)))
+
+
+def sp_release_seq(handle, seq: int, stream=None) -> None:
+    check(load().sp_release_seq(handle, seq, _stream(stream)))
+
+
+def sp_export_table(handle, seq: int, layer: int, kv_head: int, cap: int, page_size: int,
+                    stream=None):
+    np_ = c_int32()
+    ids = (c_int32 * max(cap, 1))()
+    pos = (c_int32 * max(cap * page_size, 1))()
+    check(load().sp_export_table(handle, seq, layer, kv_head, byref(np_), ids, pos, cap,
+                                 _stream(stream)))
+    n = np_.value
+    return list(ids[:n]), [list(pos[j * page_size:(j + 1) * page_size]) for j in range(n)]
+
+
+def sp_visible_count(handle, seq: int, layer: int, kv_head: int, positions: Sequence[int],
+                     stream=None) -> List[int]:
+    out = (c_int32 * max(1, len(positions)))()
+    check(load().sp_visible_count(handle, seq, layer, kv_head, i64_array(positions),
+                                  len(positions), out, _stream(stream)))
+    return list(out[:len(positions)])
+
+
+def sp_seq_len(handle, seq: int, layer: int) -> int:
+    n = c_int32()
+    check(load().sp_seq_len(handle, seq, layer, byref(n)))
+    return n.value
+
+
+def sp_free_pages(handle) -> int:
+    n = c_int32()
+    check(load().sp_free_pages(handle, byref(n)))
+    return n.value
+
+
+def sp_count_prefill_pairs(handle, seq: int, layer: int, n0: int, c: int) -> int:
+    r = c_int64()
+    check(load().sp_count_prefill_pairs(handle, seq, layer, n0, c, byref(r)))
+    return r.value
+
+
+def sp_count_decode_bytes(handle, layer: int, seq_ids: Sequence[int], t: Sequence[int]) -> int:
+    r = c_int64()
+    check(load().sp_count_decode_bytes(handle, layer, i32_array(seq_ids), len(seq_ids),
+                                       i64_array(t), byref(r)))
+    return r.value
+
+
+def sp_get_status(handle, stream=None) -> int:
+    w = c_int32()
+    check(load().sp_get_status(handle, _stream(stream), byref(w)))
+    return w.value
+
+
+def sp_last_error() -> str:
+    return load().sp_last_error().decode(errors="replace")
+
+
+# ------------------------------------------------------------ convenience class
+
+class SegPagedCache:
+    """Owns the three device buffers (torch tensors) and the library handle."""
+
+    def __init__(self, cfg: Config, device: str = "cuda"):
+        self.cfg = cfg
+        pool_b, meta_b, ws_b = sp_required_bytes(cfg)
+        # 1024-byte alignment: torch's caching allocator returns 512-byte
+        # aligned blocks, so over-allocate and offset.
+        self._pool_raw, self.pool = self._aligned(pool_b, device)
+        self._meta_raw, self.meta = self._aligned(meta_b, device)
+        self._ws_raw, self.ws = self._aligned(ws_b, device)
+        self.handle = sp_cache_create(cfg, self.pool, self.meta, self.ws)
+
+    @staticmethod
+    def _aligned(nbytes: int, device: str):
+        raw = torch.empty(nbytes + 1024, dtype=torch.uint8, device=device)
+        off = (-raw.data_ptr()) % 1024
+        return raw, raw[off:off + nbytes]
+
+    def close(self) -> None:
+        if getattr(self, "handle", None) is not None:
+            sp_cache_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # views of the page pool: [num_pages, page_size, head_dim] bf16 each
+    def k_pool(self) -> torch.Tensor:
+        c = self.cfg
+        half = c.num_pages * c.page_size * c.head_dim
+        return self.pool.view(torch.bfloat16)[:half].view(c.num_pages, c.page_size, c.head_dim)
+
+    def v_pool(self) -> torch.Tensor:
+        c = self.cfg
+        half = c.num_pages * c.page_size * c.head_dim
+        return self.pool.view(torch.bfloat16)[half:2 * half].view(c.num_pages, c.page_size, c.head_dim)
+
+    def set_policy(self, seq: int, policies, stream=None) -> None:
+        flat = []
+        for row in policies:
+            for p in row:
+                flat.append(p if isinstance(p, Policy) else Policy(*p))
+        sp_set_policy(self.handle, seq, flat, stream)
+
+    def build(self, seq: int, layer: int, k: torch.Tensor, v: torch.Tensor, stream=None) -> None:
+        assert k.dtype == torch.bfloat16 and k.is_cuda and k.stride(-1) == 1
+        n = k.shape[0]
+        sp_build_cache(self.handle, seq, layer, k, v, n, k.stride(0), stream)
+
+    def append_kv(self, layer: int, seq_ids, cu_new, k, v, stream=None) -> None:
+        assert k.is_contiguous() and v.is_contiguous()
+        sp_append_kv(self.handle, layer, seq_ids, cu_new, k, v, stream)
+
+    def prefill(self, layer: int, seq_ids, cu_q, q, k, v, out=None, lse=None, want_lse=True,
+                stream=None):
+        assert q.is_contiguous() and k.is_contiguous() and v.is_contiguous()
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None and want_lse:
+            lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
+        sp_attention_prefill(self.handle, layer, seq_ids, cu_q, q, k, v, out, lse, stream)
+        return out, lse
+
+    def decode(self, layer: int, seq_ids, q, out=None, lse=None, want_lse=True, stream=None):
+        assert q.is_contiguous()
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None and want_lse:
+            lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
+        sp_attention_decode(self.handle, layer, seq_ids, q, out, lse, stream)
+        return out, lse
+
+    def release(self, seq: int, stream=None) -> None:
+        sp_release_seq(self.handle, seq, stream)
+
+    def export_table(self, seq: int, layer: int, kv_head: int):
+        cap = (self.cfg.max_seq_len + self.cfg.page_size - 1) // self.cfg.page_size + 1
+        return sp_export_table(self.handle, seq, layer, kv_head, cap, self.cfg.page_size)
+
+    def visible_count(self, seq: int, layer: int, kv_head: int, positions) -> List[int]:
+        return sp_visible_count(self.handle, seq, layer, kv_head, positions)
+
+    def seq_len(self, seq: int, layer: int) -> int:
+        return sp_seq_len(self.handle, seq, layer)
+
+    def free_pages(self) -> int:
+        return sp_free_pages(self.handle)
+
+    def count_prefill_pairs(self, seq: int, layer: int, n0: int, c: int) -> int:
+        return sp_count_prefill_pairs(self.handle, seq, layer, n0, c)
+
+    def count_decode_bytes(self, layer: int, seq_ids, t) -> int:
+        return sp_count_decode_bytes(self.handle, layer, seq_ids, t)
+
+    def status(self, stream=None) -> int:
+        return sp_get_status(self.handle, stream)

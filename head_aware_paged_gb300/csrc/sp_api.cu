@@ -1,0 +1,607 @@
+// sp_api.cu -- host side of the C ABI declared in include/segpaged.h:
+// argument validation, the host mirror of lengths / page counts / policies,
+// device-memory layout over the caller's buffers, and kernel launches.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <memory>
+#include <mutex>
+
+#include "sp_device.cuh"
+#include "sp_internal.h"
+#include "sp_prefill.h"
+
+namespace sp {
+
+namespace {
+thread_local std::string g_last_error;
+constexpr int kMaxDecodeCtas = 1024;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Layout {
+    int32_t max_pages_unit = 0;
+    size_t pol = 0, npages = 0, seqlen = 0, ptab = 0, idx = 0, fstack = 0, status = 0,
+           meta_total = 0;
+    size_t tiles = 0, tile_ctr = 0, part_o = 0, part_ml = 0, counters = 0, scratch = 0,
+           ws_total = 0;
+    int64_t max_tiles = 0, max_parts = 0, max_counter_units = 0, scratch_ints = 0;
+    size_t pool_total = 0;
+};
+
+sp_status check_config(const sp_config* c) {
+    if (!c) return fail(SP_ERR_INVALID_ARG, "config is null");
+    if (c->num_layers < 1 || c->num_q_heads < 1 || c->num_kv_heads < 1)
+        return fail(SP_ERR_INVALID_ARG, "num_layers, num_q_heads and num_kv_heads must be >= 1");
+    if (c->num_q_heads % c->num_kv_heads != 0)
+        return fail(SP_ERR_INVALID_ARG, "num_q_heads must be a multiple of num_kv_heads");
+    if (c->num_q_heads / c->num_kv_heads > 16)
+        return fail(SP_ERR_UNSUPPORTED, "more than 16 query heads per KV head");
+    if (c->head_dim != 64 && c->head_dim != 128)
+        return fail(SP_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+    if (c->page_size != 16 && c->page_size != 32 && c->page_size != 64 && c->page_size != 128)
+        return fail(SP_ERR_UNSUPPORTED, "page_size must be 16, 32, 64 or 128");
+    if (c->max_seqs < 1 || c->max_seq_len < 1 || c->num_pages < 1 || c->max_tokens < 1 ||
+        c->max_batch < 1 || c->max_idx_per_seq < 0)
+        return fail(SP_ERR_INVALID_ARG, "capacities must be positive");
+    if ((int64_t)c->num_pages * c->page_size >= (int64_t(1) << 31))
+        return fail(SP_ERR_UNSUPPORTED, "num_pages * page_size must stay below 2^31 rows");
+    if (c->max_batch > kMaxCallSeqs)
+        return fail(SP_ERR_UNSUPPORTED, "max_batch above 512");
+    if ((int64_t)c->max_batch * c->num_kv_heads > kMaxDecodeUnits)
+        return fail(SP_ERR_UNSUPPORTED, "max_batch * num_kv_heads above 4096");
+    if ((int64_t)c->num_layers * c->num_kv_heads > kMaxPolicyUnits)
+        return fail(SP_ERR_UNSUPPORTED, "num_layers * num_kv_heads above 8192");
+    return SP_OK;
+}
+
+Layout make_layout(const sp_config* c) {
+    Layout L;
+    const int64_t S = c->max_seqs, NL = c->num_layers, H = c->num_kv_heads;
+    const int64_t units = S * NL * H;
+    L.max_pages_unit = (int32_t)((c->max_seq_len + c->page_size - 1) / c->page_size + 1);
+    size_t o = 0;
+    L.pol = o;     o = align_up(o + units * sizeof(UnitPol), 256);
+    L.npages = o;  o = align_up(o + units * 4, 256);
+    L.seqlen = o;  o = align_up(o + S * NL * 4, 256);
+    L.ptab = o;    o = align_up(o + units * (size_t)L.max_pages_unit * 4, 256);
+    L.idx = o;     o = align_up(o + S * (size_t)std::max(c->max_idx_per_seq, 1) * 4, 256);
+    L.fstack = o;  o = align_up(o + (size_t)c->num_pages * 4, 256);
+    L.status = o;  o = align_up(o + 64, 256);
+    L.meta_total = o;
+    const int group = c->num_q_heads / c->num_kv_heads;
+    L.max_tiles = prefill_max_tiles(c);
+    L.max_counter_units = (int64_t)c->max_batch * H;
+    L.max_parts = L.max_counter_units + kMaxDecodeCtas;
+    L.scratch_ints = std::max<int64_t>((int64_t)L.max_pages_unit * (1 + c->page_size), 3 * 65536);
+    o = 0;
+    L.tiles = o;    o = align_up(o + L.max_tiles * sizeof(int4), 256);
+    L.tile_ctr = o; o = align_up(o + 64, 256);
+    L.part_o = o;   o = align_up(o + L.max_parts * group * (size_t)c->head_dim * 4, 256);
+    L.part_ml = o;  o = align_up(o + L.max_parts * group * 2 * 4, 256);
+    L.counters = o; o = align_up(o + L.max_counter_units * 4, 256);
+    L.scratch = o;  o = align_up(o + L.scratch_ints * 4, 256);
+    L.ws_total = o;
+    L.pool_total = 2 * (size_t)c->num_pages * c->page_size * c->head_dim * 2;
+    return L;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool valid_seq(const sp_cache* c, int32_t seq) { return seq >= 0 && seq < c->cfg.max_seqs; }
+bool valid_layer(const sp_cache* c, int32_t l) { return l >= 0 && l < c->cfg.num_layers; }
+
+size_t unit_index(const sp_cache* c, int seq, int layer, int h) {
+    return ((size_t)seq * c->cfg.num_layers + layer) * c->cfg.num_kv_heads + h;
+}
+
+const int32_t* host_idx(const sp_cache* c, int seq, const UnitPol& u) {
+    return c->h_idx[seq].data() + u.idx_off;
+}
+
+// Shared by build and append: validate lengths, check pool capacity against
+// the host mirror, then launch the allocator and the scatter kernel.
+sp_status write_tokens(sp_cache* c, int32_t layer, const int32_t* seqs, int32_t n_seqs,
+                       const int64_t* counts, const __nv_bfloat16* k, const __nv_bfloat16* v,
+                       int64_t row_stride, cudaStream_t stream) {
+    CallSeqs cs;
+    std::memset(&cs, 0, sizeof(cs));
+    cs.n = n_seqs;
+    int64_t demand = 0, rows = 0, max_items = 0;
+    for (int b = 0; b < n_seqs; ++b) {
+        const int seq = seqs[b];
+        const int64_t n_old = c->h_seqlen[(size_t)seq * c->cfg.num_layers + layer];
+        const int64_t n_new = n_old + counts[b];
+        if (n_new > c->cfg.max_seq_len)
+            return fail(SP_ERR_INVALID_ARG, "sequence " + std::to_string(seq) +
+                                                " would exceed max_seq_len");
+        cs.seq[b] = seq;
+        cs.n_old[b] = (int32_t)n_old;
+        cs.cnt[b] = (int32_t)counts[b];
+        cs.row0[b] = (int32_t)rows;
+        rows += counts[b];
+        for (int h = 0; h < c->cfg.num_kv_heads; ++h) {
+            const UnitPol& u = c->h_pol[unit_index(c, seq, layer, h)];
+            const int32_t* idx = host_idx(c, seq, u);
+            demand += unit_pages(u, idx, n_new, c->cfg.page_size) -
+                      unit_pages(u, idx, n_old, c->cfg.page_size);
+            const ItemRanges r = retained_items(u, idx, n_old, n_new, c->cfg.page_size);
+            max_items = std::max(max_items, (r.hi[0] - r.lo[0]) + (r.hi[1] - r.lo[1]));
+        }
+    }
+    if (demand > c->h_free)
+        return fail(SP_ERR_OUT_OF_PAGES, "call needs " + std::to_string(demand) +
+                                             " pages, " + std::to_string(c->h_free) + " free");
+    if (rows == 0) return SP_OK;
+    cudaError_t e = launch_alloc(c, cs, layer, (int32_t)c->h_free, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "allocator launch");
+    e = launch_scatter(c, cs, layer, k, v, row_stride, max_items, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "scatter launch");
+    c->h_free -= demand;
+    for (int b = 0; b < n_seqs; ++b) {
+        const int seq = seqs[b];
+        c->h_seqlen[(size_t)seq * c->cfg.num_layers + layer] += (int32_t)counts[b];
+        for (int h = 0; h < c->cfg.num_kv_heads; ++h) {
+            const size_t ui = unit_index(c, seq, layer, h);
+            const UnitPol& u = c->h_pol[ui];
+            c->h_npages[ui] = (int32_t)unit_pages(u, host_idx(c, seq, u),
+                                                  c->h_seqlen[(size_t)seq * c->cfg.num_layers + layer],
+                                                  c->cfg.page_size);
+        }
+    }
+    return SP_OK;
+}
+
+sp_status check_seq_list(const sp_cache* c, const int32_t* seq_ids, int32_t n_seqs) {
+    if (!seq_ids || n_seqs < 1) return fail(SP_ERR_INVALID_ARG, "empty sequence list");
+    if (n_seqs > c->cfg.max_batch) return fail(SP_ERR_INVALID_ARG, "more sequences than max_batch");
+    std::vector<uint8_t> seen(c->cfg.max_seqs, 0);
+    for (int b = 0; b < n_seqs; ++b) {
+        const int s = seq_ids[b];
+        if (!valid_seq(c, s)) return fail(SP_ERR_INVALID_ARG, "sequence id out of range");
+        if (seen[s]) return fail(SP_ERR_INVALID_ARG, "sequence listed twice");
+        if (!c->h_policy_set[s]) return fail(SP_ERR_INVALID_ARG, "sequence has no policy");
+        seen[s] = 1;
+    }
+    return SP_OK;
+}
+
+}  // namespace
+
+sp_status fail(sp_status s, const std::string& msg) {
+    g_last_error = msg;
+    return s;
+}
+
+sp_status cuda_fail(cudaError_t e, const char* what) {
+    g_last_error = std::string(what) + ": " + cudaGetErrorString(e);
+    return SP_ERR_CUDA;
+}
+
+bool encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                    uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows, bool swizzle128,
+                    std::string* err) {
+    auto fn = get_encode();
+    if (!fn) { *err = "cuTensorMapEncodeTiled unavailable (no CUDA driver)"; return false; }
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) { *err = "cuTensorMapEncodeTiled failed, code " + std::to_string((int)r); return false; }
+    return true;
+}
+
+}  // namespace sp
+
+using namespace sp;
+
+extern "C" {
+
+const char* sp_last_error(void) { return g_last_error.c_str(); }
+
+sp_status sp_required_bytes(const sp_config* cfg, size_t* pool_bytes, size_t* meta_bytes,
+                            size_t* ws_bytes) {
+    sp_status s = check_config(cfg);
+    if (s != SP_OK) return s;
+    if (!pool_bytes || !meta_bytes || !ws_bytes) return fail(SP_ERR_INVALID_ARG, "null output");
+    const Layout L = make_layout(cfg);
+    *pool_bytes = L.pool_total;
+    *meta_bytes = L.meta_total;
+    *ws_bytes = L.ws_total;
+    return SP_OK;
+}
+
+sp_status sp_cache_create(const sp_config* cfg, void* pool, void* meta, void* ws, sp_cache** out) {
+    sp_status s = check_config(cfg);
+    if (s != SP_OK) return s;
+    if (!out) return fail(SP_ERR_INVALID_ARG, "null output handle");
+    *out = nullptr;
+    if (!pool || !meta || !ws) return fail(SP_ERR_INVALID_ARG, "null device buffer");
+    if ((reinterpret_cast<uintptr_t>(pool) | reinterpret_cast<uintptr_t>(meta) |
+         reinterpret_cast<uintptr_t>(ws)) & 1023)
+        return fail(SP_ERR_INVALID_ARG, "device buffers must be 1024-byte aligned");
+    const Layout L = make_layout(cfg);
+    sp_cache* c = new sp_cache();
+    c->cfg = *cfg;
+    Geo& g = c->geo;
+    g.layers = cfg->num_layers; g.hq = cfg->num_q_heads; g.hkv = cfg->num_kv_heads;
+    g.group = cfg->num_q_heads / cfg->num_kv_heads; g.d = cfg->head_dim; g.page = cfg->page_size;
+    g.max_seqs = cfg->max_seqs; g.max_pages_unit = L.max_pages_unit;
+    g.max_idx_per_seq = std::max(cfg->max_idx_per_seq, 1); g.num_pages = cfg->num_pages;
+    cudaError_t e = cudaGetDevice(&c->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
+    if (e != cudaSuccess) { delete c; return cuda_fail(e, "device query"); }
+    c->decode_ctas = std::min(c->num_sms, kMaxDecodeCtas);
+    const size_t pool_half = (size_t)cfg->num_pages * cfg->page_size * cfg->head_dim;
+    c->kpool = static_cast<__nv_bfloat16*>(pool);
+    c->vpool = c->kpool + pool_half;
+    uint8_t* mb = static_cast<uint8_t*>(meta);
+    c->meta.pol = reinterpret_cast<UnitPol*>(mb + L.pol);
+    c->meta.npages = reinterpret_cast<int32_t*>(mb + L.npages);
+    c->meta.seqlen = reinterpret_cast<int32_t*>(mb + L.seqlen);
+    c->meta.ptab = reinterpret_cast<int32_t*>(mb + L.ptab);
+    c->meta.idx = reinterpret_cast<int32_t*>(mb + L.idx);
+    c->meta.fstack = reinterpret_cast<int32_t*>(mb + L.fstack);
+    c->meta.status = reinterpret_cast<int32_t*>(mb + L.status);
+    uint8_t* wb = static_cast<uint8_t*>(ws);
+    c->ws.base = ws; c->ws.bytes = L.ws_total;
+    c->ws.tiles = reinterpret_cast<int4*>(wb + L.tiles); c->ws.max_tiles = L.max_tiles;
+    c->ws.tile_ctr = reinterpret_cast<int32_t*>(wb + L.tile_ctr);
+    c->ws.part_o = reinterpret_cast<float*>(wb + L.part_o);
+    c->ws.part_ml = reinterpret_cast<float*>(wb + L.part_ml);
+    c->ws.max_parts = L.max_parts;
+    c->ws.counters = reinterpret_cast<int32_t*>(wb + L.counters);
+    c->ws.max_counter_units = L.max_counter_units;
+    c->ws.scratch = reinterpret_cast<int32_t*>(wb + L.scratch);
+    c->ws.scratch_ints = L.scratch_ints;
+    std::string err;
+    const uint64_t rows = (uint64_t)cfg->num_pages * cfg->page_size;
+    if (!encode_tmap_2d(&c->tm_kpool, c->kpool, cfg->head_dim, rows, cfg->head_dim * 2, 64,
+                        cfg->page_size, true, &err) ||
+        !encode_tmap_2d(&c->tm_vpool, c->vpool, cfg->head_dim, rows, cfg->head_dim * 2, 64,
+                        cfg->page_size, true, &err)) {
+        delete c;
+        return fail(SP_ERR_CUDA, err);
+    }
+    // Device state: every page free, all units empty, the pool zeroed (slots
+    // past a page's valid range are read by the kernels and multiplied by a
+    // zero weight, so they must hold finite values).
+    e = cudaMemset(meta, 0, L.meta_total);
+    if (e == cudaSuccess) e = cudaMemset(ws, 0, L.ws_total);
+    if (e == cudaSuccess) e = cudaMemset(pool, 0, L.pool_total);
+    if (e == cudaSuccess) e = launch_init_meta(c, 0);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) { delete c; return cuda_fail(e, "cache initialisation"); }
+    const size_t units = (size_t)cfg->max_seqs * cfg->num_layers * cfg->num_kv_heads;
+    c->h_pol.assign(units, UnitPol{});
+    c->h_idx.assign(cfg->max_seqs, std::vector<int32_t>(1, 0));
+    c->h_policy_set.assign(cfg->max_seqs, 0);
+    c->h_seqlen.assign((size_t)cfg->max_seqs * cfg->num_layers, 0);
+    c->h_npages.assign(units, 0);
+    c->h_free = cfg->num_pages;
+    *out = c;
+    return SP_OK;
+}
+
+sp_status sp_cache_destroy(sp_cache* cache) {
+    if (!cache) return fail(SP_ERR_INVALID_ARG, "null handle");
+    delete cache;
+    return SP_OK;
+}
+
+sp_status sp_set_policy(sp_cache* c, int32_t seq, const sp_head_policy* p, void* stream) {
+    if (!c || !p) return fail(SP_ERR_INVALID_ARG, "null argument");
+    if (!valid_seq(c, seq)) return fail(SP_ERR_INVALID_ARG, "sequence id out of range");
+    for (int l = 0; l < c->cfg.num_layers; ++l)
+        if (c->h_seqlen[(size_t)seq * c->cfg.num_layers + l] != 0)
+            return fail(SP_ERR_INVALID_ARG, "sequence holds tokens; release it first");
+    const int NU = c->cfg.num_layers * c->cfg.num_kv_heads, P = c->cfg.page_size;
+    std::vector<UnitPol> recs(NU);
+    std::vector<int32_t> idx;
+    for (int u = 0; u < NU; ++u) {
+        const sp_head_policy& hp = p[u];
+        UnitPol r{};
+        r.kind = hp.kind;
+        if (hp.kind == SP_GLOBAL) {
+        } else if (hp.kind == SP_LOCAL) {
+            if (hp.sink < 0 || hp.window < 1)
+                return fail(SP_ERR_INVALID_ARG, "LOCAL needs sink >= 0 and window >= 1");
+            if ((int64_t)hp.window > c->cfg.max_seq_len + (int64_t)P)
+                return fail(SP_ERR_INVALID_ARG, "LOCAL window longer than max_seq_len");
+            r.sink = hp.sink;
+            r.window = hp.window;
+            r.ring = (hp.window + P - 1) / P + 1;
+            r.sink_pages = (hp.sink + P - 1) / P;
+            if ((int64_t)r.sink_pages + r.ring > (c->cfg.max_seq_len + P - 1) / P + 1 &&
+                (int64_t)hp.sink > c->cfg.max_seq_len)
+                return fail(SP_ERR_INVALID_ARG, "LOCAL sink longer than max_seq_len");
+        } else if (hp.kind == SP_RETRIEVAL) {
+            if (hp.n_idx < 0 || (hp.n_idx > 0 && !hp.idx))
+                return fail(SP_ERR_INVALID_ARG, "RETRIEVAL list missing");
+            for (int k = 0; k < hp.n_idx; ++k) {
+                if (hp.idx[k] < 0 || (k > 0 && hp.idx[k] <= hp.idx[k - 1]))
+                    return fail(SP_ERR_INVALID_ARG, "RETRIEVAL indices must be >= 0 and strictly ascending");
+            }
+            r.idx_off = (int32_t)idx.size();
+            r.n_idx = hp.n_idx;
+            idx.insert(idx.end(), hp.idx, hp.idx + hp.n_idx);
+            if ((int64_t)idx.size() > c->cfg.max_idx_per_seq)
+                return fail(SP_ERR_INVALID_ARG, "retrieval lists exceed max_idx_per_seq");
+        } else {
+            return fail(SP_ERR_INVALID_ARG, "unknown head class " + std::to_string(hp.kind));
+        }
+        recs[u] = r;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t base = unit_index(c, seq, 0, 0);
+    cudaError_t e = cudaMemcpyAsync(c->meta.pol + base, recs.data(), NU * sizeof(UnitPol),
+                                    cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess && !idx.empty())
+        e = cudaMemcpyAsync(c->meta.idx + (size_t)seq * c->geo.max_idx_per_seq, idx.data(),
+                            idx.size() * 4, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);   // host staging buffers go out of scope
+    if (e != cudaSuccess) return cuda_fail(e, "policy upload");
+    std::copy(recs.begin(), recs.end(), c->h_pol.begin() + base);
+    if (idx.empty()) idx.push_back(0);
+    c->h_idx[seq] = std::move(idx);
+    c->h_policy_set[seq] = 1;
+    return SP_OK;
+}
+
+sp_status sp_build_cache(sp_cache* c, int32_t seq, int32_t layer, const void* k, const void* v,
+                         int64_t n_tokens, int64_t row_stride, void* stream) {
+    if (!c || !k || !v) return fail(SP_ERR_INVALID_ARG, "null argument");
+    if (!valid_seq(c, seq) || !valid_layer(c, layer))
+        return fail(SP_ERR_INVALID_ARG, "sequence or layer out of range");
+    if (!c->h_policy_set[seq]) return fail(SP_ERR_INVALID_ARG, "sequence has no policy");
+    if (c->h_seqlen[(size_t)seq * c->cfg.num_layers + layer] != 0)
+        return fail(SP_ERR_INVALID_ARG, "build needs an empty (sequence, layer)");
+    if (n_tokens < 0 || n_tokens > c->cfg.max_seq_len)
+        return fail(SP_ERR_INVALID_ARG, "n_tokens outside [0, max_seq_len]");
+    if (row_stride < (int64_t)c->cfg.num_kv_heads * c->cfg.head_dim || row_stride % 8 != 0)
+        return fail(SP_ERR_INVALID_ARG, "row_stride must be >= kv_heads*head_dim and a multiple of 8");
+    if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15)
+        return fail(SP_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
+    const int64_t cnt = n_tokens;
+    return write_tokens(c, layer, &seq, 1, &cnt, static_cast<const __nv_bfloat16*>(k),
+                        static_cast<const __nv_bfloat16*>(v), row_stride,
+                        static_cast<cudaStream_t>(stream));
+}
+
+sp_status sp_append_kv(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32_t n_seqs,
+                       const int32_t* cu_new, const void* k, const void* v, void* stream) {
+    if (!c || !cu_new || !k || !v) return fail(SP_ERR_INVALID_ARG, "null argument");
+    if (!valid_layer(c, layer)) return fail(SP_ERR_INVALID_ARG, "layer out of range");
+    sp_status s = check_seq_list(c, seq_ids, n_seqs);
+    if (s != SP_OK) return s;
+    if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15)
+        return fail(SP_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
+    if (cu_new[0] != 0) return fail(SP_ERR_INVALID_ARG, "cu_new[0] must be 0");
+    std::vector<int64_t> counts(n_seqs);
+    for (int b = 0; b < n_seqs; ++b) {
+        counts[b] = (int64_t)cu_new[b + 1] - cu_new[b];
+        if (counts[b] < 0) return fail(SP_ERR_INVALID_ARG, "cu_new must be non-decreasing");
+    }
+    if (cu_new[n_seqs] > c->cfg.max_tokens)
+        return fail(SP_ERR_INVALID_ARG, "more new tokens than max_tokens");
+    return write_tokens(c, layer, seq_ids, n_seqs, counts.data(),
+                        static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v),
+                        (int64_t)c->cfg.num_kv_heads * c->cfg.head_dim,
+                        static_cast<cudaStream_t>(stream));
+}
+
+sp_status sp_attention_prefill(sp_cache* c, int32_t layer, const int32_t* seq_ids,
+                               int32_t n_seqs, const int32_t* cu_q, const void* q,
+                               const void* k, const void* v, void* out, float* lse,
+                               void* stream) {
+    if (!c || !cu_q || !q || !k || !v || !out) return fail(SP_ERR_INVALID_ARG, "null argument");
+    if (!valid_layer(c, layer)) return fail(SP_ERR_INVALID_ARG, "layer out of range");
+    sp_status s = check_seq_list(c, seq_ids, n_seqs);
+    if (s != SP_OK) return s;
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+         reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out)) & 15)
+        return fail(SP_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned");
+    if (cu_q[0] != 0) return fail(SP_ERR_INVALID_ARG, "cu_q[0] must be 0");
+    for (int b = 0; b < n_seqs; ++b) {
+        if (cu_q[b + 1] < cu_q[b]) return fail(SP_ERR_INVALID_ARG, "cu_q must be non-decreasing");
+        const int64_t n = c->h_seqlen[(size_t)seq_ids[b] * c->cfg.num_layers + layer];
+        if (n + (cu_q[b + 1] - cu_q[b]) > c->cfg.max_seq_len)
+            return fail(SP_ERR_INVALID_ARG, "chunk would pass max_seq_len");
+    }
+    if (cu_q[n_seqs] > c->cfg.max_tokens) return fail(SP_ERR_INVALID_ARG, "more rows than max_tokens");
+    return prefill_impl(c, layer, seq_ids, n_seqs, cu_q, static_cast<const __nv_bfloat16*>(q),
+                        static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v),
+                        static_cast<__nv_bfloat16*>(out), lse, static_cast<cudaStream_t>(stream));
+}
+
+sp_status sp_attention_decode(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32_t n_seqs,
+                              const void* q, void* out, float* lse, void* stream) {
+    if (!c || !q || !out) return fail(SP_ERR_INVALID_ARG, "null argument");
+    if (!valid_layer(c, layer)) return fail(SP_ERR_INVALID_ARG, "layer out of range");
+    sp_status s = check_seq_list(c, seq_ids, n_seqs);
+    if (s != SP_OK) return s;
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 3)
+        return fail(SP_ERR_INVALID_ARG, "q and out must be 4-byte aligned");
+    DecodeParams* p = new DecodeParams();   // large; keep it off the host stack
+    std::unique_ptr<DecodeParams> guard(p);
+    p->meta = c->meta;
+    p->geo = c->geo;
+    p->layer = layer;
+    p->n_seqs = n_seqs;
+    p->n_units = n_seqs * c->cfg.num_kv_heads;
+    p->item_off[0] = 0;
+    int64_t total = 0;
+    const int P = c->cfg.page_size;
+    for (int b = 0; b < n_seqs; ++b) {
+        const int seq = seq_ids[b];
+        const int64_t n = c->h_seqlen[(size_t)seq * c->cfg.num_layers + layer];
+        if (n < 1) return fail(SP_ERR_INVALID_ARG, "decode needs the query's own token appended first");
+        p->seq[b] = seq;
+        p->tq[b] = (int32_t)(n - 1);
+        for (int h = 0; h < c->cfg.num_kv_heads; ++h) {
+            const UnitPol& u = c->h_pol[unit_index(c, seq, layer, h)];
+            total += decode_items(decode_ranges(u, host_idx(c, seq, u), n - 1, P), P);
+            p->item_off[b * c->cfg.num_kv_heads + h + 1] = (int32_t)total;
+        }
+    }
+    if (total >= (int64_t(1) << 31)) return fail(SP_ERR_UNSUPPORTED, "too many pages in one call");
+    p->total_items = total;
+    p->q = static_cast<const __nv_bfloat16*>(q);
+    p->out = static_cast<__nv_bfloat16*>(out);
+    p->lse = lse;
+    p->part_o = c->ws.part_o;
+    p->part_ml = c->ws.part_ml;
+    p->counters = c->ws.counters;
+    p->scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c->cfg.head_dim));
+    cudaError_t e = launch_decode(c, *p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    return SP_OK;
+}
+
+sp_status sp_release_seq(sp_cache* c, int32_t seq, void* stream) {
+    if (!c) return fail(SP_ERR_INVALID_ARG, "null handle");
+    if (!valid_seq(c, seq)) return fail(SP_ERR_INVALID_ARG, "sequence id out of range");
+    int64_t held = 0;
+    const size_t base = unit_index(c, seq, 0, 0);
+    const int NU = c->cfg.num_layers * c->cfg.num_kv_heads;
+    for (int u = 0; u < NU; ++u) held += c->h_npages[base + u];
+    cudaError_t e = launch_release(c, seq, (int32_t)c->h_free, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "release launch");
+    c->h_free += held;
+    for (int u = 0; u < NU; ++u) c->h_npages[base + u] = 0;
+    for (int l = 0; l < c->cfg.num_layers; ++l) c->h_seqlen[(size_t)seq * c->cfg.num_layers + l] = 0;
+    return SP_OK;
+}
+
+sp_status sp_export_table(sp_cache* c, int32_t seq, int32_t layer, int32_t kv_head,
+                          int32_t* npages, int32_t* page_ids, int32_t* slot_pos, int32_t cap,
+                          void* stream) {
+    if (!c || !npages || !page_ids || !slot_pos) return fail(SP_ERR_INVALID_ARG, "null argument");
+    if (!valid_seq(c, seq) || !valid_layer(c, layer) || kv_head < 0 || kv_head >= c->cfg.num_kv_heads)
+        return fail(SP_ERR_INVALID_ARG, "unit out of range");
+    const int32_t np = c->h_npages[unit_index(c, seq, layer, kv_head)];
+    *npages = np;
+    if (np > cap) return fail(SP_ERR_INVALID_ARG, "cap smaller than the unit's page count");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t* d_ids = c->ws.scratch;
+    int32_t* d_pos = c->ws.scratch + c->geo.max_pages_unit;
+    cudaError_t e = launch_export(c, seq, layer, kv_head, d_ids, d_pos, st);
+    if (e == cudaSuccess && np > 0)
+        e = cudaMemcpyAsync(page_ids, d_ids, (size_t)np * 4, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && np > 0)
+        e = cudaMemcpyAsync(slot_pos, d_pos, (size_t)np * c->cfg.page_size * 4,
+                            cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "export");
+    return SP_OK;
+}
+
+sp_status sp_visible_count(sp_cache* c, int32_t seq, int32_t layer, int32_t kv_head,
+                           const int64_t* positions, int32_t n, int32_t* counts, void* stream) {
+    if (!c || !positions || !counts) return fail(SP_ERR_INVALID_ARG, "null argument");
+    if (!valid_seq(c, seq) || !valid_layer(c, layer) || kv_head < 0 || kv_head >= c->cfg.num_kv_heads)
+        return fail(SP_ERR_INVALID_ARG, "unit out of range");
+    if (n < 0 || n > 65536) return fail(SP_ERR_INVALID_ARG, "between 0 and 65536 positions");
+    if (n == 0) return SP_OK;
+    const int64_t held = c->h_seqlen[(size_t)seq * c->cfg.num_layers + layer];
+    for (int k = 0; k < n; ++k)
+        if (positions[k] < held - 1 || positions[k] >= held + c->cfg.max_tokens)
+            return fail(SP_ERR_INVALID_ARG, "position outside [held-1, held+max_tokens)");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int64_t* d_pos = reinterpret_cast<int64_t*>(c->ws.scratch);
+    int32_t* d_out = c->ws.scratch + 2 * 65536;
+    cudaError_t e = cudaMemcpyAsync(d_pos, positions, (size_t)n * 8, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = launch_decode_counts(c, seq, layer, kv_head, d_pos, n, d_out, st);
+    if (e == cudaSuccess) e = launch_prefill_counts(c, seq, layer, kv_head, d_pos, n, d_out, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(counts, d_out, (size_t)n * 4, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "visible count");
+    return SP_OK;
+}
+
+sp_status sp_seq_len(const sp_cache* c, int32_t seq, int32_t layer, int32_t* n) {
+    if (!c || !n) return fail(SP_ERR_INVALID_ARG, "null argument");
+    if (!valid_seq(c, seq) || !valid_layer(c, layer)) return fail(SP_ERR_INVALID_ARG, "out of range");
+    *n = c->h_seqlen[(size_t)seq * c->cfg.num_layers + layer];
+    return SP_OK;
+}
+
+sp_status sp_free_pages(const sp_cache* c, int32_t* n) {
+    if (!c || !n) return fail(SP_ERR_INVALID_ARG, "null argument");
+    *n = (int32_t)c->h_free;
+    return SP_OK;
+}
+
+sp_status sp_count_prefill_pairs(const sp_cache* c, int32_t seq, int32_t layer, int64_t n0,
+                                 int64_t cnt, int64_t* pairs) {
+    if (!c || !pairs) return fail(SP_ERR_INVALID_ARG, "null argument");
+    if (!valid_seq(c, seq) || !valid_layer(c, layer) || n0 < 0 || cnt < 0)
+        return fail(SP_ERR_INVALID_ARG, "out of range");
+    if (!c->h_policy_set[seq]) return fail(SP_ERR_INVALID_ARG, "sequence has no policy");
+    int64_t total = 0;
+    for (int h = 0; h < c->cfg.num_kv_heads; ++h) {
+        const UnitPol& u = c->h_pol[unit_index(c, seq, layer, h)];
+        const int32_t* idx = host_idx(c, seq, u);
+        int64_t s = 0;
+        if (u.kind == kGlobal) {
+            // sum_{i=n0}^{n0+cnt-1} (i + 1)
+            s = (n0 + 1 + n0 + cnt) * cnt / 2;
+        } else {
+            for (int64_t i = n0; i < n0 + cnt; ++i) s += visible_count(u, idx, i);
+        }
+        total += s * c->geo.group;
+    }
+    *pairs = total;
+    return SP_OK;
+}
+
+sp_status sp_count_decode_bytes(const sp_cache* c, int32_t layer, const int32_t* seq_ids,
+                                int32_t n_seqs, const int64_t* t, int64_t* bytes) {
+    if (!c || !seq_ids || !t || !bytes) return fail(SP_ERR_INVALID_ARG, "null argument");
+    if (!valid_layer(c, layer)) return fail(SP_ERR_INVALID_ARG, "layer out of range");
+    int64_t total = 0;
+    for (int b = 0; b < n_seqs; ++b) {
+        if (!valid_seq(c, seq_ids[b]) || !c->h_policy_set[seq_ids[b]])
+            return fail(SP_ERR_INVALID_ARG, "bad sequence");
+        for (int h = 0; h < c->cfg.num_kv_heads; ++h) {
+            const UnitPol& u = c->h_pol[unit_index(c, seq_ids[b], layer, h)];
+            total += visible_count(u, host_idx(c, seq_ids[b], u), t[b]);
+        }
+    }
+    *bytes = total * 2 * c->cfg.head_dim * 2;
+    return SP_OK;
+}
+
+sp_status sp_get_status(sp_cache* c, void* stream, int32_t* word) {
+    if (!c) return fail(SP_ERR_INVALID_ARG, "null handle");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t w = 0;
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = cudaMemcpy(&w, c->meta.status, 4, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && w != 0) e = cudaMemset(c->meta.status, 0, 4);
+    if (e != cudaSuccess) return cuda_fail(e, "status read");
+    if (word) *word = w;
+    if (w & kStatusTimeout) return fail(SP_ERR_TIMEOUT, "a device wait timed out");
+    if (w != 0) return fail(SP_ERR_DEVICE_STATUS, "device status flags " + std::to_string(w));
+    return SP_OK;
+}
+
+}  // extern "C"

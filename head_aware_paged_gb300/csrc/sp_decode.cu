@@ -1,0 +1,401 @@
+// sp_decode.cu -- split-KV decode over each head's own visible pages.
+//
+// One query per sequence reads, for every (sequence, KV head) unit, only the
+// pages holding that head's visible tokens (RedKnot SegPagedAttention runtime
+// article section 4: each head attends over its own page table, no mask;
+// section 5: decode is where the saving grows with the context).  Decode is
+// HBM-bound (KV-cache tutorial section 3.3), so the design goal is a
+// continuous, balanced page stream:
+//
+//   * The visible pages of all units of the call form one list of work items
+//     (one item = one page with a valid slot range).  The persistent grid
+//     splits that list evenly: CTA c streams items [T c / G, T (c+1) / G), so
+//     every SM reads the same number of pages whatever the head classes.
+//   * One producer lane streams the pages with 2D TMA loads (128-byte
+//     swizzle) into a ring of shared-memory stages; four consumer warps share
+//     each page (16 keys each) and compute QK^T and PV for all query heads of
+//     the KV head at once with mma.sync m16n8k16 (rows = query heads, so each
+//     K/V byte is read once for the whole GQA group), with an online softmax
+//     in registers (tutorial section 10.2) and deferred normalisation
+//     (section 10.4).
+//   * Where a unit's items span several CTAs (split-KV), each CTA writes an
+//     unnormalised partial (o, m, l); the last CTA to finish the unit (atomic
+//     ticket, no waiting) merges them: m* = max m_s, l* = sum 2^(m_s-m*) l_s,
+//     O = sum 2^(m_s-m*) o_s / l*.
+#include "sp_internal.h"
+#include "sp_device.cuh"
+
+namespace sp {
+
+namespace {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMaxGroup = 16;
+
+template <int D, int P>
+struct DecodeShape {
+    static constexpr int kHalves = D / 64;              // 128-byte column blocks per row
+    static constexpr int kHalfBytes = P * 128;
+    static constexpr int kTileBytes = kHalves * kHalfBytes;   // K (or V) of one page
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kStages = (160 * 1024 / kStageBytes) > 8 ? 8
+                                   : (160 * 1024 / kStageBytes) < 2 ? 2
+                                   : (160 * 1024 / kStageBytes);
+    static constexpr int kMergeBytes = kConsumerWarps * kMaxGroup * (D + 2) * 4;
+    static constexpr int kSmemBytes = kStages * kStageBytes + kMergeBytes
+                                      + kStages * 16 /*full, empty*/ + kStages * 16 /*desc*/
+                                      + 64 + 1024 /*alignment slack*/;
+};
+
+__device__ __forceinline__ int64_t cta_of_item(int64_t x, int64_t T, int G) {
+    return (x * G + G - 1) / T;
+}
+
+template <int D, int P>
+__global__ void __launch_bounds__(kDecodeThreads, 1)
+k_decode(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmK,
+         const __grid_constant__ CUtensorMap tmV) {
+    using S = DecodeShape<D, P>;
+    constexpr int NST = S::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* stages = smem;
+    float* merge_o = reinterpret_cast<float*>(smem + NST * S::kStageBytes);  // [4][16][D]
+    float* merge_ml = merge_o + kConsumerWarps * kMaxGroup * D;              // [4][16][2]
+    uint64_t* full = reinterpret_cast<uint64_t*>(merge_ml + kConsumerWarps * kMaxGroup * 2);
+    uint64_t* empty = full + NST;
+    int4* desc = reinterpret_cast<int4*>(empty + NST);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(desc + NST);
+    int* flag_last = const_cast<int*>(abort_flag) + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = gridDim.x, c = blockIdx.x;
+    const int64_t T = p.total_items;
+    const int64_t x0 = T * c / G, x1 = T * (c + 1) / G;
+    const Geo& g = p.geo;
+    const int group = g.group;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NST; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], kConsumerWarps); }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kConsumerWarps) {
+        // ---------------- producer: stream this CTA's pages ----------------
+        if (lane == 0 && x0 < x1) {
+            prefetch_tmap(&tmK);
+            prefetch_tmap(&tmV);
+            int u = 0;
+            {   // first unit with item_off[u+1] > x0
+                int lo = 0, hi = p.n_units - 1;
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (p.item_off[mid + 1] <= x0) lo = mid + 1; else hi = mid;
+                }
+                u = lo;
+            }
+            int64_t issued = 0;
+            for (int64_t x = x0; x < x1; ++x) {
+                while (p.item_off[u + 1] <= x) ++u;
+                const int b = u / g.hkv, h = u % g.hkv;
+                const int seq = p.seq[b];
+                const int64_t row = g.unit_row(seq, p.layer, h);
+                const UnitPol pol = p.meta.pol[row];
+                const int32_t* idx = p.meta.idx + (int64_t)seq * g.max_idx_per_seq + pol.idx_off;
+                const SlotRanges rg = decode_ranges(pol, idx, p.tq[b], P);
+                int64_t j = x - p.item_off[u];
+                int64_t pidx = 0, lo = 0, hi = 0;
+                for (int q = 0; q < rg.count; ++q) {
+                    const int64_t np = range_pages(rg.lo[q], rg.hi[q], P);
+                    if (j < np) {
+                        pidx = rg.lo[q] / P + j;
+                        lo = max64(rg.lo[q], pidx * P) - pidx * P;
+                        hi = min64(rg.hi[q], (pidx + 1) * P) - pidx * P;
+                        break;
+                    }
+                    j -= np;
+                }
+                int32_t page = p.meta.ptab[row * g.max_pages_unit + pidx];
+                if (page < 0 || page >= g.num_pages) {
+                    atomicOr(p.meta.status, kStatusBadPage);
+                    page = 0; lo = hi = 0;              // load something harmless, use nothing
+                }
+                const int64_t k = (x - x0) / NST;
+                const int s = (int)((x - x0) % NST);
+                if (k > 0 && !mbar_wait(&empty[s], (uint32_t)((k - 1) & 1), abort_flag, p.meta.status))
+                    break;
+                desc[s] = make_int4(u, (int)lo, (int)hi, 0);
+                mbar_arrive_expect_tx(&full[s], S::kStageBytes);
+                uint8_t* kdst = stages + s * S::kStageBytes;
+                uint8_t* vdst = kdst + S::kTileBytes;
+                #pragma unroll
+                for (int hh = 0; hh < S::kHalves; ++hh) {
+                    tma_load_2d(kdst + hh * S::kHalfBytes, &tmK, &full[s], hh * 64, page * P);
+                    tma_load_2d(vdst + hh * S::kHalfBytes, &tmV, &full[s], hh * 64, page * P);
+                }
+                ++issued;
+            }
+            // Leave only after every load this CTA issued has landed (bounded,
+            // also after an abort).
+            for (int s = 0; s < NST && s < issued; ++s) {
+                const int64_t last_k = (issued - 1 - s) / NST;
+                mbar_wait(&full[s], (uint32_t)(last_k & 1), nullptr, nullptr);
+            }
+        }
+        return;
+    }
+
+    // ------------------------------ consumers ------------------------------
+    const int ctid = threadIdx.x;     // 0..127
+    // Units with no visible token: O = 0, LSE = -inf (one CTA each).
+    for (int u = c; u < p.n_units; u += G) {
+        if (p.item_off[u + 1] != p.item_off[u]) continue;
+        const int b = u / g.hkv, h = u % g.hkv;
+        for (int e = ctid; e < group * D; e += kConsumerWarps * 32) {
+            const int r = e / D, col = e % D;
+            p.out[((int64_t)b * g.hq + h * group + r) * D + col] = __float2bfloat16(0.f);
+            if (col == 0 && p.lse) p.lse[(int64_t)b * g.hq + h * group + r] = -INFINITY;
+        }
+    }
+    if (x0 >= x1) return;
+
+    const int qr = lane >> 2, qc = (lane & 3) * 2;   // fragment row / column base
+    uint32_t qa[D / 16][4];
+    float m_run[2], l_run[2];
+    float o_acc[D / 8][4];
+    int cur_u = -1;
+
+    for (int64_t x = x0; x < x1; ++x) {
+        const int s = (int)((x - x0) % NST);
+        const int64_t k = (x - x0) / NST;
+        if (!mbar_wait(&full[s], (uint32_t)(k & 1), abort_flag, p.meta.status)) break;
+        const int4 dd = desc[s];
+        const int u = dd.x, lo = dd.y, hi = dd.z;
+        const int b = u / g.hkv, h = u % g.hkv;
+        if (u != cur_u) {
+            cur_u = u;
+            const __nv_bfloat16* qb = p.q + ((int64_t)b * g.hq + h * group) * D;
+            #pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const int col = kk * 16 + qc;
+                auto ld = [&](int r, int cc) -> uint32_t {
+                    return r < group ? *reinterpret_cast<const uint32_t*>(qb + (int64_t)r * D + cc) : 0u;
+                };
+                qa[kk][0] = ld(qr, col);
+                qa[kk][1] = ld(qr + 8, col);
+                qa[kk][2] = ld(qr, col + 8);
+                qa[kk][3] = ld(qr + 8, col + 8);
+            }
+            m_run[0] = m_run[1] = -INFINITY;
+            l_run[0] = l_run[1] = 0.f;
+            #pragma unroll
+            for (int nt = 0; nt < D / 8; ++nt)
+                #pragma unroll
+                for (int e = 0; e < 4; ++e) o_acc[nt][e] = 0.f;
+        }
+        const uint32_t kbase = smem_u32(stages + s * S::kStageBytes);
+        const uint32_t vbase = kbase + S::kTileBytes;
+        for (int sub = warp; sub < P / 16; sub += kConsumerWarps) {
+            const int key0 = sub * 16;
+            if (key0 >= hi || key0 + 16 <= lo) continue;
+            // S = Q K^T for 16 keys: two n-tiles of 8 keys
+            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            {
+                const int mi = lane >> 3;
+                const uint32_t key = key0 + (lane & 7) + (mi >= 2 ? 8 : 0);
+                #pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t chunk = kk * 2 + (mi & 1);
+                    const uint32_t addr = kbase + (chunk >> 3) * S::kHalfBytes + sw128(key, chunk & 7);
+                    uint32_t r0, r1, r2, r3;
+                    ldsm_x4(addr, r0, r1, r2, r3);
+                    mma_bf16_16816(sc[0], qa[kk], r0, r1);
+                    mma_bf16_16816(sc[1], qa[kk], r2, r3);
+                }
+            }
+            // scale to log2 units, mask keys outside [lo, hi), online softmax
+            float mx[2] = {-INFINITY, -INFINITY};
+            #pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+                #pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int key = key0 + nt * 8 + qc + (e & 1);
+                    float v = sc[nt][e] * p.scale_log2;
+                    if (key < lo || key >= hi) v = -INFINITY;
+                    sc[nt][e] = v;
+                    mx[e >> 1] = fmaxf(mx[e >> 1], v);
+                }
+            #pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+            }
+            float alpha[2], mbase[2];
+            #pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const float m_new = fmaxf(m_run[r], mx[r]);
+                mbase[r] = m_new == -INFINITY ? 0.f : m_new;
+                alpha[r] = fast_exp2(m_run[r] - mbase[r]);
+                m_run[r] = m_new;
+            }
+            float psum[2] = {0.f, 0.f};
+            #pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+                #pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float pv = fast_exp2(sc[nt][e] - mbase[e >> 1]);
+                    sc[nt][e] = pv;
+                    psum[e >> 1] += pv;
+                }
+            #pragma unroll
+            for (int r = 0; r < 2; ++r) l_run[r] = l_run[r] * alpha[r] + psum[r];
+            #pragma unroll
+            for (int nt = 0; nt < D / 8; ++nt) {
+                o_acc[nt][0] *= alpha[0]; o_acc[nt][1] *= alpha[0];
+                o_acc[nt][2] *= alpha[1]; o_acc[nt][3] *= alpha[1];
+            }
+            // O += P V: P from the S fragments (rows = heads, k = keys)
+            uint32_t pa[4];
+            pa[0] = pack_bf16(sc[0][0], sc[0][1]);
+            pa[1] = pack_bf16(sc[0][2], sc[0][3]);
+            pa[2] = pack_bf16(sc[1][0], sc[1][1]);
+            pa[3] = pack_bf16(sc[1][2], sc[1][3]);
+            {
+                const int mi = lane >> 3;
+                const uint32_t key = key0 + (lane & 7) + ((mi & 1) ? 8 : 0);
+                #pragma unroll
+                for (int np = 0; np < D / 16; ++np) {
+                    const uint32_t chunk = np * 2 + (mi >> 1);
+                    const uint32_t addr = vbase + (chunk >> 3) * S::kHalfBytes + sw128(key, chunk & 7);
+                    uint32_t r0, r1, r2, r3;
+                    ldsm_x4_t(addr, r0, r1, r2, r3);
+                    mma_bf16_16816(o_acc[2 * np], pa, r0, r1);
+                    mma_bf16_16816(o_acc[2 * np + 1], pa, r2, r3);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+
+        const bool unit_ends = (x + 1 == x1) || (p.item_off[u + 1] == x + 1);
+        if (!unit_ends) continue;
+
+        // ------------- merge the four warps' partial states -------------
+        #pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
+            l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
+        }
+        #pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int row = qr + 8 * r;
+            if (row < group) {
+                float* mo = merge_o + ((size_t)warp * kMaxGroup + row) * D;
+                #pragma unroll
+                for (int nt = 0; nt < D / 8; ++nt) {
+                    mo[nt * 8 + qc] = o_acc[nt][2 * r];
+                    mo[nt * 8 + qc + 1] = o_acc[nt][2 * r + 1];
+                }
+                if ((lane & 3) == 0) {
+                    merge_ml[(warp * kMaxGroup + row) * 2] = m_run[r];
+                    merge_ml[(warp * kMaxGroup + row) * 2 + 1] = l_run[r];
+                }
+            }
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32));
+
+        const int64_t ia = p.item_off[u], ib = p.item_off[u + 1];
+        const int c_first = (int)cta_of_item(ia, T, G), c_last = (int)cta_of_item(ib - 1, T, G);
+        const bool whole = c_first == c_last;
+        const int64_t part = (int64_t)u + c;
+        for (int e = ctid; e < group * D; e += kConsumerWarps * 32) {
+            const int r = e / D, col = e % D;
+            float mst = -INFINITY;
+            #pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) mst = fmaxf(mst, merge_ml[(w * kMaxGroup + r) * 2]);
+            float lst = 0.f, ost = 0.f;
+            #pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float sc_w = fast_exp2(merge_ml[(w * kMaxGroup + r) * 2] - mst);
+                lst += sc_w * merge_ml[(w * kMaxGroup + r) * 2 + 1];
+                ost += sc_w * merge_o[((size_t)w * kMaxGroup + r) * D + col];
+            }
+            const int64_t orow = (int64_t)b * g.hq + h * group + r;
+            if (whole) {
+                p.out[orow * D + col] = __float2bfloat16(ost / lst);
+                if (col == 0 && p.lse) p.lse[orow] = (mst + __log2f(lst)) * 0.69314718055994531f;
+            } else {
+                p.part_o[(part * group + r) * D + col] = ost;
+                if (col == 0) {
+                    p.part_ml[(part * group + r) * 2] = mst;
+                    p.part_ml[(part * group + r) * 2 + 1] = lst;
+                }
+            }
+        }
+        if (!whole) {
+            __threadfence();
+            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32));
+            if (ctid == 0) {
+                int target = 0;
+                for (int cc = c_first; cc <= c_last; ++cc)
+                    target += (T * cc / G) < (T * (cc + 1) / G) ? 1 : 0;
+                const int old = atomicAdd(&p.counters[u], 1);
+                *flag_last = (old == target - 1) ? 1 : 0;
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32));
+            if (*flag_last) {
+                __threadfence();
+                for (int e = ctid; e < group * D; e += kConsumerWarps * 32) {
+                    const int r = e / D, col = e % D;
+                    float mst = -INFINITY;
+                    for (int cc = c_first; cc <= c_last; ++cc) {
+                        if (!((T * cc / G) < (T * (cc + 1) / G))) continue;
+                        mst = fmaxf(mst, __ldcg(&p.part_ml[(((int64_t)u + cc) * group + r) * 2]));
+                    }
+                    float lst = 0.f, ost = 0.f;
+                    for (int cc = c_first; cc <= c_last; ++cc) {
+                        if (!((T * cc / G) < (T * (cc + 1) / G))) continue;
+                        const int64_t pi = (int64_t)u + cc;
+                        const float w = fast_exp2(__ldcg(&p.part_ml[(pi * group + r) * 2]) - mst);
+                        lst += w * __ldcg(&p.part_ml[(pi * group + r) * 2 + 1]);
+                        ost += w * __ldcg(&p.part_o[(pi * group + r) * D + col]);
+                    }
+                    const int64_t orow = (int64_t)b * g.hq + h * group + r;
+                    p.out[orow * D + col] = __float2bfloat16(ost / lst);
+                    if (col == 0 && p.lse) p.lse[orow] = (mst + __log2f(lst)) * 0.69314718055994531f;
+                }
+                if (ctid == 0) p.counters[u] = 0;
+            }
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32));
+    }
+}
+
+template <int D, int P>
+cudaError_t launch_decode_t(const sp_cache* c, const DecodeParams& p, int grid, cudaStream_t s) {
+    using Sh = DecodeShape<D, P>;
+    cudaError_t e = cudaFuncSetAttribute(k_decode<D, P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Sh::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    k_decode<D, P><<<grid, kDecodeThreads, Sh::kSmemBytes, s>>>(p, c->tm_kpool, c->tm_vpool);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const sp_cache* c, const DecodeParams& p, cudaStream_t s) {
+    int grid = c->decode_ctas;
+    if (p.total_items < grid) grid = (int)(p.total_items > 0 ? p.total_items : 1);
+    const int D = c->geo.d, P = c->geo.page;
+#define SP_DEC(DD, PP) if (D == DD && P == PP) return launch_decode_t<DD, PP>(c, p, grid, s);
+    SP_DEC(64, 16) SP_DEC(64, 32) SP_DEC(64, 64) SP_DEC(64, 128)
+    SP_DEC(128, 16) SP_DEC(128, 32) SP_DEC(128, 64) SP_DEC(128, 128)
+#undef SP_DEC
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace sp

@@ -1,0 +1,126 @@
+// sp_internal.h -- handle, device-memory layout and launcher declarations
+// shared by the host API (sp_api.cu) and the kernel files.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "../../include/segpaged.h"
+#include "sp_rules.h"
+
+namespace sp {
+
+constexpr int kMaxCallSeqs = 512;     // sequences in one call (kernel parameters)
+constexpr int kMaxDecodeUnits = 4096; // (sequence, KV head) units in one decode call
+constexpr int kMaxPolicyUnits = 8192; // layers * kv heads
+
+// Device pointers into the caller's meta buffer.
+struct Meta {
+    UnitPol* pol;        // [max_seqs][layers][hkv]
+    int32_t* npages;     // [max_seqs][layers][hkv]
+    int32_t* seqlen;     // [max_seqs][layers]
+    int32_t* ptab;       // [max_seqs][layers][hkv][max_pages_unit]
+    int32_t* idx;        // [max_seqs][max_idx_per_seq]
+    int32_t* fstack;     // [num_pages] free-page stack
+    int32_t* status;     // [8]: 0 = status word, 1 = stack top (debug mirror)
+};
+
+// Geometry every kernel needs.
+struct Geo {
+    int32_t layers, hq, hkv, group, d, page, max_seqs, max_pages_unit,
+            max_idx_per_seq, num_pages;
+    __host__ __device__ int64_t unit_row(int seq, int layer, int h) const {
+        return ((int64_t)seq * layers + layer) * hkv + h;
+    }
+};
+
+// Per-call list of sequences (kernel parameter).
+struct CallSeqs {
+    int32_t n;
+    int32_t seq[kMaxCallSeqs];   // sequence slot
+    int32_t n_old[kMaxCallSeqs]; // tokens held before the call
+    int32_t cnt[kMaxCallSeqs];   // new tokens / query rows
+    int32_t row0[kMaxCallSeqs];  // first row in the call's packed tensors
+};
+
+struct DecodeParams {
+    Meta meta;
+    Geo geo;
+    int32_t layer;
+    int32_t n_seqs;
+    int32_t n_units;             // n_seqs * hkv
+    int64_t total_items;         // pages streamed, all units
+    int32_t seq[kMaxCallSeqs];
+    int32_t tq[kMaxCallSeqs];    // query position per sequence
+    int32_t item_off[kMaxDecodeUnits + 1];
+    const __nv_bfloat16* q;
+    __nv_bfloat16* out;
+    float* lse;
+    float* part_o;               // [(n_units + grid)][group][d]
+    float* part_ml;              // [(n_units + grid)][group][2]
+    int32_t* counters;           // [n_units], zero between calls
+    float scale_log2;            // log2(e) / sqrt(d)
+};
+
+struct Workspace {
+    void* base;
+    size_t bytes;
+    // regions
+    int4* tiles;          int64_t max_tiles;
+    int32_t* tile_ctr;
+    float* part_o;        float* part_ml;  int64_t max_parts;
+    int32_t* counters;    int64_t max_counter_units;
+    int32_t* scratch;     int64_t scratch_ints;   // export / visible-count staging
+};
+
+}  // namespace sp
+
+struct sp_cache {
+    sp_config cfg;
+    sp::Geo geo;
+    int device = 0;
+    int num_sms = 0;
+    int decode_ctas = 0;
+    __nv_bfloat16* kpool = nullptr;
+    __nv_bfloat16* vpool = nullptr;
+    sp::Meta meta;
+    sp::Workspace ws;
+    CUtensorMap tm_kpool;   // [num_pages*P rows][d], box {64 or d, P}, 128B swizzle
+    CUtensorMap tm_vpool;
+    // host mirror (authoritative for lengths, page counts and policies)
+    std::vector<sp::UnitPol> h_pol;              // [max_seqs][layers][hkv]
+    std::vector<std::vector<int32_t>> h_idx;     // per sequence, CSR by unit
+    std::vector<uint8_t> h_policy_set;           // per sequence
+    std::vector<int32_t> h_seqlen;               // [max_seqs][layers]
+    std::vector<int32_t> h_npages;               // [max_seqs][layers][hkv]
+    int64_t h_free = 0;
+};
+
+namespace sp {
+
+// Error plumbing (sp_api.cu).
+sp_status fail(sp_status s, const std::string& msg);
+sp_status cuda_fail(cudaError_t e, const char* what);
+bool encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                    uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows,
+                    bool swizzle128, std::string* err);
+
+// Launchers (return the launch's cudaError_t).
+cudaError_t launch_init_meta(const sp_cache* c, cudaStream_t s);
+cudaError_t launch_alloc(const sp_cache* c, const CallSeqs& cs, int layer, int32_t top,
+                         cudaStream_t s);
+cudaError_t launch_scatter(const sp_cache* c, const CallSeqs& cs, int layer,
+                           const __nv_bfloat16* k, const __nv_bfloat16* v,
+                           int64_t row_stride, int64_t max_items, cudaStream_t s);
+cudaError_t launch_release(const sp_cache* c, int seq, int32_t top, cudaStream_t s);
+cudaError_t launch_export(const sp_cache* c, int seq, int layer, int h, int32_t* out_ids,
+                          int32_t* out_pos, cudaStream_t s);
+cudaError_t launch_decode_counts(const sp_cache* c, int seq, int layer, int h,
+                                 const int64_t* pos, int n, int32_t* out, cudaStream_t s);
+cudaError_t launch_decode(const sp_cache* c, const DecodeParams& p, cudaStream_t s);
+
+}  // namespace sp

@@ -1,0 +1,166 @@
+// sp_plan.h -- the key tiles one prefill work item attends over.
+//
+// A work item is 128 consecutive query rows (positions i_lo .. i_hi) of one
+// or two query heads of one KV head.  Its visible keys (the union of V(i)
+// over its rows) are covered by "segments" -- runs of keys from one source:
+//   * chunk: the call's own K/V rows, positions p >= n_b (rows of the chunk);
+//   * paged: unit slots of the cache pages (history, positions < n_b).
+// Each segment is cut into tiles of at most 128 keys; a tile's MMA width is
+// its valid key count rounded up to 16 (so a 4-token sink costs a 16-wide
+// tile, not 128).  Segments never overlap, so every visible key is counted
+// exactly once, and keys a tile holds that a row must not see are masked:
+//   * chunk tiles (GLOBAL / LOCAL): position p0 + c, mask by arithmetic;
+//   * paged tiles and RETRIEVAL chunk tiles: per-key position table.
+// A tile is "full" when every row of the item sees every key of it; only
+// tiles that are not full are masked.  The same functions run on the host
+// (work estimates, ordering) and in the kernels.
+#pragma once
+#include "sp_rules.h"
+
+namespace sp {
+
+constexpr int kTileKeys = 128;
+constexpr int kMaxSegs = 5;
+
+struct Seg {
+    int32_t paged;     // 0 = chunk positions, 1 = unit slots in pages
+    int32_t sinkseg;   // LOCAL sink segment (history slots are all visible)
+    int64_t start;     // first position (chunk) or first unit slot (paged, page aligned)
+    int64_t len;       // keys (chunk) or slots (paged)
+};
+
+struct Plan {
+    int nseg;
+    Seg seg[kMaxSegs];
+    int64_t ntiles;
+};
+
+struct KvTile {
+    int32_t paged;
+    int32_t nvalid;    // keys in the tile that belong to the segment
+    int32_t nkeys;     // MMA width: nvalid rounded up to 16
+    int32_t full;      // every row sees every valid key; no mask needed
+    int32_t table;     // mask needs a per-key position table
+    int64_t start;     // position of key 0 (chunk) or unit slot of key 0 (paged)
+};
+
+SP_HD void plan_push(Plan& pl, int paged, int sinkseg, int64_t start, int64_t len) {
+    if (len <= 0) return;
+    Seg& s = pl.seg[pl.nseg++];
+    s.paged = paged; s.sinkseg = sinkseg; s.start = start; s.len = len;
+    pl.ntiles += (len + kTileKeys - 1) / kTileKeys;
+}
+
+// Segments of one work item.  n_b: tokens the unit already holds (history);
+// rows i_lo .. i_hi (positions, i_lo >= n_b).
+SP_HD Plan make_plan(const UnitPol& u, const int32_t* idx, int64_t n_b, int64_t i_lo,
+                     int64_t i_hi, int P) {
+    Plan pl;
+    pl.nseg = 0;
+    pl.ntiles = 0;
+    if (u.kind == kGlobal) {
+        plan_push(pl, 1, 0, 0, n_b);
+        plan_push(pl, 0, 0, n_b, i_hi + 1 - n_b);
+    } else if (u.kind == kLocal) {
+        const int64_t se = min64(u.sink, i_hi + 1);            // sink positions [0, se)
+        plan_push(pl, 1, 1, 0, min64(se, n_b));
+        if (se > n_b) plan_push(pl, 0, 0, n_b, se - n_b);
+        const int64_t wa = max64(u.sink, i_lo - u.window + 1);  // window positions [wa, i_hi]
+        if (wa < n_b && wa <= i_hi) {
+            const int64_t e = min64(i_hi + 1, n_b);
+            const int64_t ring = u.ring, base = (int64_t)u.sink_pages * P;
+            const int64_t qa = (wa - u.sink) % (ring * P);
+            const int64_t fa = qa / P;
+            const int64_t np = (qa + (e - wa) - 1) / P - fa + 1;  // ring pages touched (<= ring)
+            const int64_t n1 = min64(np, ring - fa);
+            plan_push(pl, 1, 0, base + fa * P, n1 * P);
+            if (np > n1) plan_push(pl, 1, 0, base, (np - n1) * P);
+        }
+        const int64_t ca = max64(wa, n_b);
+        if (ca <= i_hi) plan_push(pl, 0, 0, ca, i_hi + 1 - ca);
+    } else {
+        const int64_t cnt_h = count_below(idx, u.n_idx, n_b);
+        plan_push(pl, 1, 0, 0, cnt_h);
+        if (cnt_h < u.n_idx && idx[cnt_h] <= i_hi) {
+            const int64_t f = idx[cnt_h];
+            plan_push(pl, 0, 0, f, i_hi + 1 - f);
+        }
+    }
+    return pl;
+}
+
+// Tile t (0 <= t < pl.ntiles) of a plan.
+SP_HD KvTile plan_tile(const Plan& pl, const UnitPol& u, int64_t t, int64_t i_lo,
+                       int64_t i_hi) {
+    KvTile k;
+    k.paged = 0; k.nvalid = 0; k.nkeys = 0; k.full = 0; k.table = 0; k.start = 0;
+    for (int s = 0; s < pl.nseg; ++s) {
+        const Seg& g = pl.seg[s];
+        const int64_t nt = (g.len + kTileKeys - 1) / kTileKeys;
+        if (t >= nt) { t -= nt; continue; }
+        k.paged = g.paged;
+        k.start = g.start + t * kTileKeys;
+        k.nvalid = (int32_t)min64(kTileKeys, g.len - t * kTileKeys);
+        k.nkeys = (k.nvalid + 15) & ~15;
+        const bool exact = k.nkeys == k.nvalid;
+        if (g.paged) {
+            // history: every stored position is < n_b <= i_lo; GLOBAL and
+            // RETRIEVAL slots and LOCAL sink slots are visible to all rows
+            k.full = exact && (u.kind != kLocal || g.sinkseg);
+            k.table = !k.full;
+        } else {
+            const int64_t p0 = k.start, p1 = k.start + k.nvalid - 1;
+            bool full = exact && p1 <= i_lo && u.kind != kRetrieval;
+            if (u.kind == kLocal) full = full && (p1 < u.sink || p0 >= i_hi - u.window + 1);
+            k.full = full;
+            k.table = u.kind == kRetrieval;
+        }
+        return k;
+    }
+    return k;
+}
+
+// Position of key c of a tile, as the mask sees it (-1 = never visible).
+SP_HD int64_t tile_key_position(const KvTile& k, const UnitPol& u, const int32_t* idx,
+                                int64_t n_b, int c, int P) {
+    if (c >= k.nvalid) return -1;
+    if (k.paged) return slot_position(u, idx, k.start + c, n_b, P);
+    const int64_t p = k.start + c;
+    if (u.kind == kRetrieval) {
+        const int64_t r = count_below(idx, u.n_idx, p);
+        return (r < u.n_idx && idx[r] == p) ? p : -1;
+    }
+    return p;
+}
+
+// Does query position i see key position p (p >= 0) under the unit's class.
+SP_HD bool sees(const UnitPol& u, int64_t p, int64_t i) {
+    if (p < 0 || p > i) return false;
+    if (u.kind == kLocal) return p < u.sink || p > i - u.window;
+    return true;
+}
+
+// Is key c of tile k visible to the query at position i?  table_pos is the
+// key's entry of the position table (used only when k.table is set).
+template <typename I>
+SP_HD bool key_visible(const KvTile& k, const UnitPol& u, I i, int c, I table_pos) {
+    if (c >= k.nvalid) return false;
+    if (k.full) return true;
+    const I p = k.table ? table_pos : (I)k.start + (I)c;
+    if (p < 0 || p > i) return false;
+    if (u.kind == kLocal) return p < (I)u.sink || p > i - (I)u.window;
+    return true;
+}
+
+// Work estimate of an item (keys times MMA width), for ordering.
+SP_HD int64_t plan_cost(const Plan& pl) {
+    int64_t c = 0;
+    for (int s = 0; s < pl.nseg; ++s) {
+        const int64_t full_tiles = pl.seg[s].len / kTileKeys;
+        const int64_t rest = pl.seg[s].len - full_tiles * kTileKeys;
+        c += full_tiles * kTileKeys + ((rest + 15) & ~15) + (rest > 0 ? 32 : 0) + 32 * full_tiles;
+    }
+    return c;
+}
+
+}  // namespace sp

@@ -1,0 +1,564 @@
+// sp_prefill.cu -- mask-free causal prefill over each head's own visible keys
+// (RedKnot SegPagedAttention runtime article section 4: every (query head, KV
+// head) pair attends over exactly its own tokens in one fused varlen call, no
+// attention mask is built).  The FlashAttention forward recurrence follows the
+// KV-cache tutorial section 10.2 (tiling with an online softmax) and 10.4
+// (normalise once at the end); its Hopper FA-3 kernel is prior art only.
+//
+// sm_103a design (one persistent CTA per SM, 12 warps):
+//   warp 0       TMA producer: the work item's Q tiles (128 rows of one or two
+//                query heads of one KV head), then its K/V tiles from the
+//                chunk (2D tensor map) or from cache pages (tensor map over
+//                the page pool), 128-byte swizzled, into a ring of stages.
+//   warp 1       TMEM owner and tcgen05 MMA issuer (one thread): S_t = Q_t K^T
+//                into TMEM, later O_t += P_t V with P_t from shared memory.
+//   warps 4-7    softmax + epilogue of query tile 0; warps 8-11 of tile 1.
+//                Each thread owns one query row: it reads its S row from
+//                TMEM, masks (only on tiles that need it, see sp_plan.h),
+//                keeps the running max / sum, writes P (bf16) into shared
+//                memory in the MMA operand layout, and rescales its O row in
+//                TMEM only when the max grew by more than 2^8 (lazy rescale).
+//   The two query tiles share every K/V tile and ping-pong on the tensor core:
+//   while one softmax group works, the MMA warp runs the other's PV and next QK.
+// Work items are cost-sorted on the host and dealt round-robin to the CTAs.
+// Every wait is bounded (sp_device.cuh); on a time-out the CTA drains its
+// copies and MMAs, frees TMEM and returns with the status word set.
+#include <algorithm>
+#include <cmath>
+#include <memory>
+#include <vector>
+
+#include "sp_device.cuh"
+#include "sp_internal.h"
+#include "sp_plan.h"
+#include "sp_prefill.h"
+#include "sp_tcgen05.cuh"
+
+namespace sp {
+
+namespace {
+
+constexpr int kPfThreads = 384;
+constexpr int kSmemLimit = 232448;     // 227 KB per CTA
+constexpr int kTmemCols = 512;
+constexpr float kRescaleLog2 = 8.0f;   // lazy-rescale threshold (log2 units)
+
+struct PrefillParams {
+    Meta meta;
+    Geo geo;
+    int32_t layer;
+    int32_t nq;                  // query tiles per item: 2 (head pairs) or 1
+    int32_t n_items;
+    float scale_log2;            // log2(e) / sqrt(d)
+    const int4* items;           // {b, kv head, head pair, row block}
+    __nv_bfloat16* out;
+    float* lse;
+    int32_t seq[kMaxCallSeqs];
+    int32_t n_b[kMaxCallSeqs];   // tokens held before the chunk
+    int32_t cnt[kMaxCallSeqs];   // chunk rows
+    int32_t row0[kMaxCallSeqs];  // first chunk row in q / k / v
+};
+
+template <int D>
+struct PfShape {
+    static constexpr int kHalves = D / 64;
+    static constexpr int kHalfBytes = 128 * 128;            // 128 rows x 128 bytes
+    static constexpr int kQBytes = kHalves * kHalfBytes;     // one Q tile
+    static constexpr int kPBytes = 2 * kHalfBytes;           // one P tile (128 x 128 bf16)
+    static constexpr int kKVBytes = kHalves * kHalfBytes;    // one K or V tile
+    static constexpr int kFixed = 2 * kQBytes + 2 * kPBytes;
+    static constexpr int kMisc = 2048;                       // barriers, flags, alignment slack
+    static constexpr int kStagesFit = (kSmemLimit - kFixed - kMisc) / kKVBytes;
+    static constexpr int kStages = kStagesFit > 6 ? 6 : kStagesFit;
+    static constexpr int kSmem = kFixed + kStages * kKVBytes + kMisc;
+    static_assert(kStages >= 2, "not enough shared memory for two K/V stages");
+};
+
+struct Item {
+    int b, kvh, h0, rows;
+    int64_t n_b, i_lo, i_hi, row_base;   // row_base: chunk row of query row 0
+    int64_t key_row0;                    // chunk row of position n_b
+    UnitPol pol;
+    const int32_t* idx;
+    const int32_t* ptab;
+};
+
+__device__ __forceinline__ Item load_item(const PrefillParams& p, int n) {
+    const int4 it = p.items[n];
+    Item m;
+    m.b = it.x;
+    m.kvh = it.y;
+    const Geo& g = p.geo;
+    m.h0 = it.y * g.group + it.z * p.nq;
+    const int seq = p.seq[m.b];
+    const int r0 = it.w * 128;
+    m.rows = min(128, p.cnt[m.b] - r0);
+    m.n_b = p.n_b[m.b];
+    m.i_lo = m.n_b + r0;
+    m.i_hi = m.i_lo + m.rows - 1;
+    m.key_row0 = p.row0[m.b];
+    m.row_base = p.row0[m.b] + r0;
+    const int64_t urow = g.unit_row(seq, p.layer, m.kvh);
+    m.pol = p.meta.pol[urow];
+    m.idx = p.meta.idx + (int64_t)seq * g.max_idx_per_seq + m.pol.idx_off;
+    m.ptab = p.meta.ptab + urow * g.max_pages_unit;
+    return m;
+}
+
+template <int D, int P>
+__global__ void __launch_bounds__(kPfThreads, 1)
+k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tmQ,
+          const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+          const __grid_constant__ CUtensorMap tmKp, const __grid_constant__ CUtensorMap tmVp) {
+    using S = PfShape<D>;
+    constexpr int NS = S::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sQ = smem;                               // [2][halves][128][128 B]
+    uint8_t* sP = sQ + 2 * S::kQBytes;                // [2][2][128][128 B]
+    uint8_t* sKV = sP + 2 * S::kPBytes;               // [NS][halves][128][128 B]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + NS * S::kKVBytes);
+    uint64_t* q_full = bars;
+    uint64_t* q_empty = bars + 1;
+    uint64_t* kv_full = bars + 2;
+    uint64_t* kv_empty = kv_full + NS;
+    uint64_t* s_full = kv_empty + NS;                 // [2]
+    uint64_t* p_full = s_full + 2;                    // [2]
+    uint64_t* o_full = p_full + 2;                    // [2]
+    uint64_t* o_empty = o_full + 2;                   // [2]
+    uint64_t* mma_done = o_empty + 2;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mma_done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    int* status = p.meta.status;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = gridDim.x, cta = blockIdx.x;
+    const Geo& g = p.geo;
+    const int nq = p.nq;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
+        for (int s = 0; s < NS; ++s) { mbar_init(&kv_full[s], 1); mbar_init(&kv_empty[s], 1); }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&s_full[t], 1);
+            mbar_init(&p_full[t], 128);
+            mbar_init(&o_full[t], 1);
+            mbar_init(&o_empty[t], 128);
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------ producer ------------------------------
+        prefetch_tmap(&tmQ); prefetch_tmap(&tmK); prefetch_tmap(&tmV);
+        prefetch_tmap(&tmKp); prefetch_tmap(&tmVp);
+        uint32_t q_loads = 0, L = 0;
+        bool ok = true;
+        for (int n = cta; n < p.n_items && ok; n += G) {
+            const Item it = load_item(p, n);
+            const Plan pl = make_plan(it.pol, it.idx, it.n_b, it.i_lo, it.i_hi, P);
+            if (pl.ntiles == 0) continue;
+            if (q_loads > 0 && !mbar_wait(q_empty, (q_loads - 1) & 1, abort_flag, status)) { ok = false; break; }
+            mbar_arrive_expect_tx(q_full, nq * S::kQBytes);
+            for (int t = 0; t < nq; ++t)
+                for (int hf = 0; hf < S::kHalves; ++hf)
+                    tma_load_2d(sQ + t * S::kQBytes + hf * S::kHalfBytes, &tmQ, q_full,
+                                (it.h0 + t) * D + hf * 64, (int32_t)it.row_base);
+            ++q_loads;
+            for (int64_t j = 0; j < pl.ntiles && ok; ++j) {
+                const KvTile kt = plan_tile(pl, it.pol, j, it.i_lo, it.i_hi);
+                for (int kv = 0; kv < 2; ++kv) {
+                    const uint32_t st = L % NS, rd = L / NS;
+                    if (rd > 0 && !mbar_wait(&kv_empty[st], (rd - 1) & 1, abort_flag, status)) { ok = false; break; }
+                    uint8_t* dst = sKV + st * S::kKVBytes;
+                    if (!kt.paged) {
+                        mbar_arrive_expect_tx(&kv_full[st], S::kKVBytes);
+                        const int32_t y = (int32_t)(it.key_row0 + (kt.start - it.n_b));
+                        for (int hf = 0; hf < S::kHalves; ++hf)
+                            tma_load_2d(dst + hf * S::kHalfBytes, kv ? &tmV : &tmK, &kv_full[st],
+                                        it.kvh * D + hf * 64, y);
+                    } else {
+                        const int np = (kt.nkeys + P - 1) / P;
+                        mbar_arrive_expect_tx(&kv_full[st], np * P * 128 * S::kHalves);
+                        for (int pg = 0; pg < np; ++pg) {
+                            int32_t phys = it.ptab[kt.start / P + pg];
+                            if (phys < 0 || phys >= g.num_pages) { atomicOr(status, kStatusBadPage); phys = 0; }
+                            for (int hf = 0; hf < S::kHalves; ++hf)
+                                tma_load_2d(dst + hf * S::kHalfBytes + pg * P * 128, kv ? &tmVp : &tmKp,
+                                            &kv_full[st], hf * 64, phys * P);
+                        }
+                    }
+                    ++L;
+                }
+            }
+        }
+        // drain: every copy issued has landed before the CTA may exit
+        for (uint32_t s = 0; s < NS && s < L; ++s)
+            mbar_wait(&kv_full[s], ((L - 1 - s) / NS) & 1, nullptr, nullptr);
+        if (q_loads > 0) mbar_wait(q_full, (q_loads - 1) & 1, nullptr, nullptr);
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------ MMA issuer ------------------------------
+        const uint32_t q_addr = smem_u32(sQ), p_addr = smem_u32(sP), kv_addr = smem_u32(sKV);
+        const uint32_t idesc_pv = idesc_bf16(128, D, true);
+        auto issue_qk = [&](int t, uint32_t st, int nkeys) {
+            const uint32_t idesc = idesc_bf16(128, nkeys, false);
+            #pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const uint32_t off = (ks >> 2) * S::kHalfBytes + (ks & 3) * 32;
+                const uint64_t a = sdesc_sw128(q_addr + t * S::kQBytes + off, 16, 1024);
+                const uint64_t b = sdesc_sw128(kv_addr + st * S::kKVBytes + off, 16, 1024);
+                tc_mma(tmem + t * 128, a, b, idesc, ks > 0 ? 1u : 0u);
+            }
+        };
+        auto issue_pv = [&](int t, uint32_t st, int nkeys, bool acc) {
+            for (int ks = 0; ks < nkeys / 16; ++ks) {
+                const uint64_t a = sdesc_sw128(p_addr + t * S::kPBytes + (ks >> 2) * S::kHalfBytes +
+                                               (ks & 3) * 32, 16, 1024);
+                const uint64_t b = sdesc_sw128(kv_addr + st * S::kKVBytes + ks * 2048,
+                                               S::kHalfBytes, 1024);
+                tc_mma(tmem + 256 + t * D, a, b, idesc_pv, (acc || ks > 0) ? 1u : 0u);
+            }
+        };
+        uint32_t q_uses = 0, L = 0, e = 0;
+        uint32_t tiles_t[2] = {0, 0};
+        bool ok = true;
+        for (int n = cta; n < p.n_items && ok; n += G) {
+            const Item it = load_item(p, n);
+            const Plan pl = make_plan(it.pol, it.idx, it.n_b, it.i_lo, it.i_hi, P);
+            const int64_t nt = pl.ntiles;
+            if (nt == 0) continue;
+            if (!mbar_wait(q_full, q_uses & 1, abort_flag, status)) { ok = false; break; }
+            ++q_uses;
+            KvTile kt = plan_tile(pl, it.pol, 0, it.i_lo, it.i_hi);
+            uint32_t stK = L % NS;
+            if (!mbar_wait(&kv_full[stK], (L / NS) & 1, abort_flag, status)) { ok = false; break; }
+            ++L;
+            tc_fence_after();
+            for (int t = 0; t < nq; ++t) { issue_qk(t, stK, kt.nkeys); tc_commit(&s_full[t]); }
+            tc_commit(&kv_empty[stK]);
+            if (nt == 1) tc_commit(q_empty);
+            for (int64_t j = 0; j < nt && ok; ++j) {
+                const uint32_t stV = L % NS;
+                if (!mbar_wait(&kv_full[stV], (L / NS) & 1, abort_flag, status)) { ok = false; break; }
+                ++L;
+                KvTile kn = kt;
+                uint32_t stK2 = 0;
+                if (j + 1 < nt) {
+                    kn = plan_tile(pl, it.pol, j + 1, it.i_lo, it.i_hi);
+                    stK2 = L % NS;
+                    if (!mbar_wait(&kv_full[stK2], (L / NS) & 1, abort_flag, status)) { ok = false; break; }
+                    ++L;
+                }
+                for (int t = 0; t < nq && ok; ++t) {
+                    if (!mbar_wait(&p_full[t], tiles_t[t] & 1, abort_flag, status)) { ok = false; break; }
+                    if (j == 0 && e > 0 &&
+                        !mbar_wait(&o_empty[t], (e - 1) & 1, abort_flag, status)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_pv(t, stV, kt.nkeys, j > 0);
+                    tc_commit(&o_full[t]);
+                    ++tiles_t[t];
+                    if (j + 1 < nt) { issue_qk(t, stK2, kn.nkeys); tc_commit(&s_full[t]); }
+                }
+                if (!ok) break;
+                tc_commit(&kv_empty[stV]);
+                if (j + 1 < nt) {
+                    tc_commit(&kv_empty[stK2]);
+                    if (j + 2 == nt) tc_commit(q_empty);
+                }
+                kt = kn;
+            }
+            ++e;
+        }
+        // all MMAs issued by this thread complete before TMEM can be freed
+        tc_commit(mma_done);
+        mbar_wait(mma_done, 0, nullptr, nullptr);
+    } else if (warp >= 4) {
+        // --------------------------- softmax + epilogue ---------------------------
+        const int t = (warp - 4) >> 2;
+        if (t < nq) {
+            const int r = threadIdx.x - (4 + 4 * t) * 32;             // query row in the tile
+            const uint32_t lane_off = ((uint32_t)(warp & 3) * 32u) << 16;
+            const uint32_t tS = tmem + lane_off + t * 128;
+            const uint32_t tO = tmem + lane_off + 256 + t * D;
+            uint8_t* myP = sP + t * S::kPBytes;
+            const float sl2 = p.scale_log2;
+            uint32_t k = 0;
+            bool ok = true;
+            for (int n = cta; n < p.n_items && ok; n += G) {
+                const Item it = load_item(p, n);
+                const Plan pl = make_plan(it.pol, it.idx, it.n_b, it.i_lo, it.i_hi, P);
+                const int head = it.h0 + t;
+                const bool row_ok = r < it.rows;
+                const int32_t i = (int32_t)(it.i_lo + r);
+                __nv_bfloat16* orow = p.out + ((it.row_base + r) * g.hq + head) * D;
+                if (pl.ntiles == 0) {
+                    if (row_ok) {
+                        for (int c = 0; c < D; c += 8)
+                            *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
+                        if (p.lse) p.lse[(it.row_base + r) * g.hq + head] = -INFINITY;
+                    }
+                    continue;
+                }
+                float m = -INFINITY, l = 0.f;
+                for (int64_t j = 0; j < pl.ntiles; ++j, ++k) {
+                    const KvTile kt = plan_tile(pl, it.pol, j, it.i_lo, it.i_hi);
+                    const bool masked = !kt.full;
+                    int32_t tpos[4] = {-1, -1, -1, -1};
+                    if (masked && kt.table) {
+                        #pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4)
+                            tpos[q4] = (int32_t)tile_key_position(kt, it.pol, it.idx, it.n_b,
+                                                                  lane + 32 * q4, P);
+                    }
+                    if (!mbar_wait(&s_full[t], k & 1, abort_flag, status)) { ok = false; break; }
+                    tc_fence_after();
+                    uint32_t sr[128];
+                    if (kt.nkeys == 128) {
+                        tmem_ld128(tS, sr);
+                    } else {
+                        #pragma unroll
+                        for (int ch = 0; ch < 8; ++ch)
+                            if (ch * 16 < kt.nkeys)
+                                tmem_ld16(tS + ch * 16, *reinterpret_cast<uint32_t(*)[16]>(&sr[ch * 16]));
+                    }
+                    // scale to log2 units, mask, tile max
+                    float tmax = -INFINITY;
+                    #pragma unroll
+                    for (int c = 0; c < 128; ++c) {
+                        if (c < kt.nkeys) {
+                            float s = __uint_as_float(sr[c]) * sl2;
+                            if (masked) {
+                                const int32_t tp = kt.table ? __shfl_sync(0xffffffffu, tpos[c >> 5], c & 31) : 0;
+                                if (!key_visible<int32_t>(kt, it.pol, i, c, tp)) s = -INFINITY;
+                            }
+                            sr[c] = __float_as_uint(s);
+                            tmax = fmaxf(tmax, s);
+                        }
+                    }
+                    // online softmax with lazy rescale
+                    float alpha = 1.f;
+                    bool resc = false;
+                    const float m_new = fmaxf(m, tmax);
+                    if (m == -INFINITY) {
+                        m = m_new;
+                    } else if (m_new > m + kRescaleLog2) {
+                        alpha = fast_exp2(m - m_new);
+                        m = m_new;
+                        resc = true;
+                    }
+                    const float mb = m == -INFINITY ? 0.f : m;
+                    float rs = 0.f;
+                    #pragma unroll
+                    for (int c = 0; c < 128; ++c) {
+                        if (c < kt.nkeys) {
+                            const float pv = fast_exp2(__uint_as_float(sr[c]) - mb);
+                            rs += pv;
+                            sr[c] = __float_as_uint(pv);
+                        }
+                    }
+                    l = l * alpha + rs;
+                    // PV of the previous tile must be done before P is overwritten
+                    // and before O is rescaled
+                    if (k > 0) {
+                        if (!mbar_wait(&o_full[t], (k - 1) & 1, abort_flag, status)) { ok = false; break; }
+                        tc_fence_after();
+                    }
+                    if (__any_sync(0xffffffffu, resc)) {
+                        #pragma unroll
+                        for (int ch = 0; ch < D / 16; ++ch) {
+                            uint32_t o[16];
+                            tmem_ld16(tO + ch * 16, o);
+                            #pragma unroll
+                            for (int e2 = 0; e2 < 16; ++e2)
+                                o[e2] = __float_as_uint(__uint_as_float(o[e2]) * alpha);
+                            tmem_st16(tO + ch * 16, o);
+                        }
+                        tmem_st_wait();
+                    }
+                    // P row -> shared memory, K-major 128-byte-swizzled operand layout
+                    #pragma unroll
+                    for (int c8 = 0; c8 < 16; ++c8) {
+                        if (c8 * 8 < kt.nkeys) {
+                            uint4 v;
+                            v.x = pack_bf16(__uint_as_float(sr[c8 * 8 + 0]), __uint_as_float(sr[c8 * 8 + 1]));
+                            v.y = pack_bf16(__uint_as_float(sr[c8 * 8 + 2]), __uint_as_float(sr[c8 * 8 + 3]));
+                            v.z = pack_bf16(__uint_as_float(sr[c8 * 8 + 4]), __uint_as_float(sr[c8 * 8 + 5]));
+                            v.w = pack_bf16(__uint_as_float(sr[c8 * 8 + 6]), __uint_as_float(sr[c8 * 8 + 7]));
+                            *reinterpret_cast<uint4*>(myP + (c8 >> 3) * S::kHalfBytes +
+                                                      sw128((uint32_t)r, (uint32_t)(c8 & 7))) = v;
+                        }
+                    }
+                    fence_async_smem();
+                    tc_fence_before();
+                    mbar_arrive(&p_full[t]);
+                }
+                if (!ok) break;
+                // epilogue: O / l -> bf16 rows, LSE
+                if (!mbar_wait(&o_full[t], (k - 1) & 1, abort_flag, status)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t orr[D];
+                if constexpr (D == 128) tmem_ld128(tO, orr); else tmem_ld64(tO, orr);
+                tc_fence_before();
+                mbar_arrive(&o_empty[t]);
+                if (row_ok) {
+                    const float inv = l > 0.f ? 1.f / l : 0.f;
+                    #pragma unroll
+                    for (int c = 0; c < D; c += 8) {
+                        uint4 v;
+                        v.x = pack_bf16(__uint_as_float(orr[c + 0]) * inv, __uint_as_float(orr[c + 1]) * inv);
+                        v.y = pack_bf16(__uint_as_float(orr[c + 2]) * inv, __uint_as_float(orr[c + 3]) * inv);
+                        v.z = pack_bf16(__uint_as_float(orr[c + 4]) * inv, __uint_as_float(orr[c + 5]) * inv);
+                        v.w = pack_bf16(__uint_as_float(orr[c + 6]) * inv, __uint_as_float(orr[c + 7]) * inv);
+                        *reinterpret_cast<uint4*>(orow + c) = v;
+                    }
+                    if (p.lse)
+                        p.lse[(it.row_base + r) * g.hq + head] =
+                            l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// |V(i)| as the tile plan and the mask see it (one thread per position).
+__global__ void k_prefill_counts(Meta meta, Geo g, int seq, int layer, int h,
+                                 const int64_t* pos, int npos, int32_t* out) {
+    const int64_t urow = g.unit_row(seq, layer, h);
+    const UnitPol pol = meta.pol[urow];
+    const int32_t* idx = meta.idx + (int64_t)seq * g.max_idx_per_seq + pol.idx_off;
+    const int64_t held = meta.seqlen[(int64_t)seq * g.layers + layer];
+    for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < npos; k += gridDim.x * blockDim.x) {
+        const int64_t i = pos[k];
+        if (i < held) continue;
+        const int64_t i_lo = held + (i - held) / 128 * 128;
+        const int64_t i_hi = i_lo + 127;
+        const Plan pl = make_plan(pol, idx, held, i_lo, i_hi, g.page);
+        int64_t cnt = 0;
+        for (int64_t t = 0; t < pl.ntiles; ++t) {
+            const KvTile kt = plan_tile(pl, pol, t, i_lo, i_hi);
+            for (int c = 0; c < kt.nkeys; ++c) {
+                const int64_t tp = kt.table ? tile_key_position(kt, pol, idx, held, c, g.page) : 0;
+                cnt += key_visible<int64_t>(kt, pol, i, c, tp) ? 1 : 0;
+            }
+        }
+        out[k] = (int32_t)cnt;
+    }
+}
+
+template <int D, int P>
+cudaError_t launch_prefill_t(const sp_cache* c, const PrefillParams& p, int grid,
+                             const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                             cudaStream_t s) {
+    using Sh = PfShape<D>;
+    cudaError_t e = cudaFuncSetAttribute(k_prefill<D, P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Sh::kSmem);
+    if (e != cudaSuccess) return e;
+    k_prefill<D, P><<<grid, kPfThreads, Sh::kSmem, s>>>(p, tq, tk, tv, c->tm_kpool, c->tm_vpool);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int64_t prefill_max_tiles(const sp_config* c) {
+    return ((int64_t)c->max_tokens / 128 + c->max_batch + 1) * c->num_q_heads;
+}
+
+sp_status prefill_impl(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32_t n_seqs,
+                       const int32_t* cu_q, const __nv_bfloat16* q, const __nv_bfloat16* k,
+                       const __nv_bfloat16* v, __nv_bfloat16* out, float* lse,
+                       cudaStream_t stream) {
+    const int T = cu_q[n_seqs];
+    if (T == 0) return SP_OK;
+    std::unique_ptr<PrefillParams> pp(new PrefillParams());
+    PrefillParams& p = *pp;
+    p.meta = c->meta;
+    p.geo = c->geo;
+    p.layer = layer;
+    const int group = c->geo.group;
+    p.nq = (group % 2 == 0) ? 2 : 1;
+    const int pairs = group / p.nq;
+    p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c->cfg.head_dim));
+    p.out = out;
+    p.lse = lse;
+    struct Cand { int64_t cost; int4 item; };
+    std::vector<Cand> cands;
+    const int P = c->cfg.page_size;
+    for (int b = 0; b < n_seqs; ++b) {
+        const int seq = seq_ids[b];
+        const int64_t n_b = c->h_seqlen[(size_t)seq * c->cfg.num_layers + layer];
+        const int cb = cu_q[b + 1] - cu_q[b];
+        p.seq[b] = seq;
+        p.n_b[b] = (int32_t)n_b;
+        p.cnt[b] = cb;
+        p.row0[b] = cu_q[b];
+        for (int h = 0; h < c->cfg.num_kv_heads; ++h) {
+            const size_t ui = ((size_t)seq * c->cfg.num_layers + layer) * c->cfg.num_kv_heads + h;
+            const UnitPol& u = c->h_pol[ui];
+            const int32_t* idx = c->h_idx[seq].data() + u.idx_off;
+            for (int rb = 0; rb * 128 < cb; ++rb) {
+                const int64_t i_lo = n_b + rb * 128;
+                const int64_t i_hi = n_b + std::min(cb, rb * 128 + 128) - 1;
+                const Plan pl = make_plan(u, idx, n_b, i_lo, i_hi, P);
+                const int64_t cost = plan_cost(pl) + 64;
+                for (int pr = 0; pr < pairs; ++pr) cands.push_back({cost, make_int4(b, h, pr, rb)});
+            }
+        }
+    }
+    if ((int64_t)cands.size() > c->ws.max_tiles)
+        return fail(SP_ERR_UNSUPPORTED, "prefill work list larger than the workspace");
+    std::stable_sort(cands.begin(), cands.end(),
+                     [](const Cand& a, const Cand& b2) { return a.cost > b2.cost; });
+    std::vector<int4> items(cands.size());
+    for (size_t n = 0; n < cands.size(); ++n) items[n] = cands[n].item;
+    p.items = c->ws.tiles;
+    p.n_items = (int32_t)items.size();
+    cudaError_t e = cudaMemcpyAsync(c->ws.tiles, items.data(), items.size() * sizeof(int4),
+                                    cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill work list upload");
+    CUtensorMap tq, tk, tv;
+    std::string err;
+    const int D = c->cfg.head_dim;
+    if (!encode_tmap_2d(&tq, q, (uint64_t)c->cfg.num_q_heads * D, T,
+                        (uint64_t)c->cfg.num_q_heads * D * 2, 64, 128, true, &err) ||
+        !encode_tmap_2d(&tk, k, (uint64_t)c->cfg.num_kv_heads * D, T,
+                        (uint64_t)c->cfg.num_kv_heads * D * 2, 64, 128, true, &err) ||
+        !encode_tmap_2d(&tv, v, (uint64_t)c->cfg.num_kv_heads * D, T,
+                        (uint64_t)c->cfg.num_kv_heads * D * 2, 64, 128, true, &err))
+        return fail(SP_ERR_CUDA, err);
+    const int grid = (int)std::min<int64_t>(c->num_sms, (int64_t)items.size());
+#define SP_PF(DD, PP) \
+    if (D == DD && P == PP) e = launch_prefill_t<DD, PP>(c, p, grid, tq, tk, tv, stream); else
+    SP_PF(64, 16) SP_PF(64, 32) SP_PF(64, 64) SP_PF(64, 128)
+    SP_PF(128, 16) SP_PF(128, 32) SP_PF(128, 64) SP_PF(128, 128)
+    e = cudaErrorInvalidValue;
+#undef SP_PF
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    return SP_OK;
+}
+
+cudaError_t launch_prefill_counts(const sp_cache* c, int seq, int layer, int h,
+                                  const int64_t* pos, int n, int32_t* out, cudaStream_t s) {
+    k_prefill_counts<<<(n + 127) / 128, 128, 0, s>>>(c->meta, c->geo, seq, layer, h, pos, n, out);
+    return cudaGetLastError();
+}
+
+}  // namespace sp

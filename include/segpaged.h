@@ -1,0 +1,207 @@
+/*
+ * segpaged.h -- C ABI of libsegpaged.so, a head-aware paged KV cache with
+ * mask-free attention for one GB300 GPU (sm_103a).
+ *
+ * Method: RedKnot SegPagedAttention, as described in the runtime article
+ * "How different attention heads see different context" (section 1: why heads
+ * may see different context; section 2: the per-(layer, KV head) head
+ * classes; section 3: per-head page tables over one physical page pool, local
+ * heads trimmed at KV-write time; section 4: one mask-free fused varlen
+ * attention over every (query head, KV head) pair's own visible tokens; section
+ * 5: the page layout must be built at write time and reused, never rebuilt per
+ * attention call) and in the RedKnot news summary (head-class sparsification:
+ * globals about 12-15 % of heads; the BUILDSTATE / SELECTVISIBLESTATE /
+ * EXECUTE split of the runtime).
+ *
+ * Conventions for every call
+ *   - Every function returns an sp_status; nothing else crosses the ABI.  On
+ *     any status other than SP_OK, sp_last_error() holds a one-line message
+ *     (thread-local) and, for argument or capacity errors, nothing was
+ *     modified and nothing was launched.
+ *   - Device memory belongs to the caller.  The library never allocates
+ *     device memory: the caller allocates the pool, metadata and workspace
+ *     buffers sized by sp_required_bytes() and keeps them alive until
+ *     sp_cache_destroy().  Tensor arguments are borrowed until the
+ *     stream-ordered work of the call has completed.
+ *   - `stream` is a cudaStream_t (0 = legacy default stream).  Calls are
+ *     asynchronous unless marked "synchronous".  All calls that touch one
+ *     cache must be issued in stream order (one stream, or with events).
+ *   - One cache handle must not be used from two host threads at once.
+ *   - Tensors are bf16 (2-byte elements), row-major and contiguous unless a
+ *     stride is given:  q / out [tokens][num_q_heads][head_dim];
+ *     k / v [tokens][num_kv_heads][head_dim]; lse [tokens][num_q_heads] fp32
+ *     (natural logarithm of the softmax denominator incl. the max shift;
+ *     -inf for a query with no visible token, whose output row is 0).
+ *   - Query head h belongs to KV head h / (num_q_heads / num_kv_heads)
+ *     (grouped-query attention, KV-cache tutorial section 5.3, 0-indexed).
+ *   - Per call order for one layer and chunk: sp_attention_prefill (history
+ *     pages + the chunk itself) then sp_append_kv (the chunk); for decode:
+ *     sp_append_kv (the new token) then sp_attention_decode.
+ */
+#ifndef SEGPAGED_H
+#define SEGPAGED_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum sp_status {
+    SP_OK = 0,
+    SP_ERR_INVALID_ARG = 1,    /* bad argument; nothing modified            */
+    SP_ERR_OUT_OF_PAGES = 2,   /* pool too small for this call; nothing modified */
+    SP_ERR_UNSUPPORTED = 3,    /* shape or size this build does not handle  */
+    SP_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed          */
+    SP_ERR_DEVICE_STATUS = 5,  /* a kernel flagged an impossible state       */
+    SP_ERR_TIMEOUT = 6         /* a bounded device wait gave up              */
+} sp_status;
+
+/* Head classes (runtime article section 2).  DENSE attends like GLOBAL; its
+ * difference (full re-prefill on reuse) lies outside attention. */
+typedef enum sp_kind { SP_GLOBAL = 0, SP_LOCAL = 1, SP_RETRIEVAL = 2 } sp_kind;
+
+/* One (layer, KV head) policy.
+ *   GLOBAL:        query i sees positions 0..i.
+ *   LOCAL:         query i sees [0, min(sink, i+1)) and [max(0, i-window+1), i];
+ *                  sink >= 0, window >= 1.
+ *   RETRIEVAL:     query i sees idx[k] <= i; idx strictly ascending, >= 0,
+ *                  n_idx >= 0; idx is a host pointer read during the call. */
+typedef struct sp_head_policy {
+    int32_t kind;
+    int32_t sink;
+    int32_t window;
+    int32_t n_idx;
+    const int32_t* idx;
+} sp_head_policy;
+
+typedef struct sp_config {
+    int32_t num_layers;
+    int32_t num_q_heads;
+    int32_t num_kv_heads;      /* num_q_heads % num_kv_heads == 0, group <= 16 */
+    int32_t head_dim;          /* 64 or 128 */
+    int32_t page_size;         /* tokens per page: 16, 32, 64 or 128 */
+    int32_t max_seqs;          /* sequence slots 0 .. max_seqs-1 */
+    int32_t max_seq_len;       /* longest context a sequence may reach */
+    int32_t num_pages;         /* physical pages in the pool (all units share it) */
+    int32_t max_idx_per_seq;   /* RETRIEVAL index capacity per sequence (all its units) */
+    int32_t max_tokens;        /* most query rows in one prefill / append call */
+    int32_t max_batch;         /* most sequences in one call */
+} sp_config;
+
+typedef struct sp_cache sp_cache;  /* opaque host handle */
+
+/* Bytes of the three caller-owned device buffers for cfg (host only, no GPU).
+ *   pool: K pages then V pages, each [num_pages][page_size][head_dim] bf16.
+ *   meta: page tables, policies, retrieval lists, free-page stack, status.
+ *   ws:   per-call scratch (prefill work list, decode split partials). */
+sp_status sp_required_bytes(const sp_config* cfg, size_t* pool_bytes,
+                            size_t* meta_bytes, size_t* ws_bytes);
+
+/* Create a handle over caller-owned buffers (each 1024-byte aligned, at least
+ * the sizes above, on the current CUDA device).  Initialises meta (all units
+ * empty, every page free) and waits for that to finish: synchronous. */
+sp_status sp_cache_create(const sp_config* cfg, void* pool, void* meta, void* ws,
+                          sp_cache** out);
+
+/* Free the host handle only; the caller frees its device buffers. */
+sp_status sp_cache_destroy(sp_cache* cache);
+
+/* BUILDSTATE, step 1 (runtime article section 2): set the policy of every
+ * (layer, KV head) of sequence `seq`; p has num_layers * num_kv_heads entries,
+ * layer-major.  The sequence must hold no tokens (fresh or released).  Copies
+ * the retrieval lists to the device on `stream`. */
+sp_status sp_set_policy(sp_cache* cache, int32_t seq, const sp_head_policy* p,
+                        void* stream);
+
+/* BUILDSTATE, step 2 (runtime article section 3, build from dense K/V, trimming
+ * local heads to their visible tokens): write positions 0 .. n_tokens-1 of
+ * (seq, layer) from dense k, v laid out [n_tokens][num_kv_heads][head_dim]
+ * with `row_stride` elements between consecutive tokens (>= kv_heads*head_dim,
+ * multiple of 8).  The (seq, layer) must be empty.  Pages are allocated in
+ * this call; only retained rows are copied. */
+sp_status sp_build_cache(sp_cache* cache, int32_t seq, int32_t layer,
+                         const void* k, const void* v, int64_t n_tokens,
+                         int64_t row_stride, void* stream);
+
+/* Append cu_new[b+1] - cu_new[b] new tokens to (seq_ids[b], layer) for
+ * b < n_seqs; k, v [cu_new[n_seqs]][num_kv_heads][head_dim] contiguous.
+ * GLOBAL heads store every token, LOCAL heads write sink slots or overwrite the
+ * oldest ring slot, RETRIEVAL heads store only listed positions.  seq_ids and
+ * cu_new are host arrays; sequences must be distinct. */
+sp_status sp_append_kv(sp_cache* cache, int32_t layer, const int32_t* seq_ids,
+                       int32_t n_seqs, const int32_t* cu_new, const void* k,
+                       const void* v, void* stream);
+
+/* EXECUTE, prefill (runtime article section 4): causal attention of a chunk.
+ * Rows cu_q[b] .. cu_q[b+1]-1 of q belong to sequence seq_ids[b] and sit at
+ * absolute positions n_b .. n_b + c_b - 1, where n_b is what (seq, layer)
+ * already holds; keys below n_b come from the cache pages, the rest from the
+ * chunk's own k, v (same row layout as q's rows, num_kv_heads heads).  Each
+ * query head attends over exactly its KV head's visible set; no mask tensor.
+ * out [cu_q[n_seqs]][num_q_heads][head_dim] bf16; lse nullable.  Does not
+ * modify the cache: call sp_append_kv with the same k, v afterwards. */
+sp_status sp_attention_prefill(sp_cache* cache, int32_t layer,
+                               const int32_t* seq_ids, int32_t n_seqs,
+                               const int32_t* cu_q, const void* q,
+                               const void* k, const void* v, void* out,
+                               float* lse, void* stream);
+
+/* EXECUTE, decode: one query per sequence at position t = n - 1, where n is
+ * what (seq_ids[b], layer) holds (its own token was appended first).
+ * q, out [n_seqs][num_q_heads][head_dim]; lse [n_seqs][num_q_heads] nullable.
+ * Split-KV: the visible pages of all units are streamed by persistent CTAs;
+ * partial results are merged in the same launch. */
+sp_status sp_attention_decode(sp_cache* cache, int32_t layer,
+                              const int32_t* seq_ids, int32_t n_seqs,
+                              const void* q, void* out, float* lse, void* stream);
+
+/* Return every page of `seq` (all layers) to the free stack and empty it; the
+ * policy stays set. */
+sp_status sp_release_seq(sp_cache* cache, int32_t seq, void* stream);
+
+/* SELECTVISIBLESTATE, for tests: the device page table of one unit.
+ * Synchronous.  Writes *npages, page_ids[npages] (physical page ids) and
+ * slot_pos[npages * page_size] (token position held by each slot, -1 if
+ * empty), as the device-side slot rules see them.  cap bounds both arrays
+ * (in pages); SP_ERR_INVALID_ARG if the unit holds more. */
+sp_status sp_export_table(sp_cache* cache, int32_t seq, int32_t layer,
+                          int32_t kv_head, int32_t* npages, int32_t* page_ids,
+                          int32_t* slot_pos, int32_t cap, void* stream);
+
+/* For tests: |V(i)| of one unit for n host positions, computed on the device
+ * by the same visible-range functions the attention kernels use.  A position
+ * must be below what the unit holds plus max_tokens.  Synchronous. */
+sp_status sp_visible_count(sp_cache* cache, int32_t seq, int32_t layer,
+                           int32_t kv_head, const int64_t* positions, int32_t n,
+                           int32_t* counts, void* stream);
+
+/* Host-side mirrors, no GPU work: tokens held by (seq, layer); free pages. */
+sp_status sp_seq_len(const sp_cache* cache, int32_t seq, int32_t layer, int32_t* n);
+sp_status sp_free_pages(const sp_cache* cache, int32_t* n);
+
+/* Work accounting from the host policy mirror (no GPU work):
+ *   visible (query, key) pairs of a prefill of rows n0 .. n0+c-1 of (seq, layer),
+ *   summed over query heads (FLOP = 4 * head_dim * pairs);
+ *   visible K+V bytes one decode query at position t of each listed sequence
+ *   reads in `layer`. */
+sp_status sp_count_prefill_pairs(const sp_cache* cache, int32_t seq, int32_t layer,
+                                 int64_t n0, int64_t c, int64_t* pairs);
+sp_status sp_count_decode_bytes(const sp_cache* cache, int32_t layer,
+                                const int32_t* seq_ids, int32_t n_seqs,
+                                const int64_t* t, int64_t* bytes);
+
+/* Synchronise `stream` and read the device status word: SP_OK, or
+ * SP_ERR_DEVICE_STATUS / SP_ERR_TIMEOUT if a kernel flagged a problem (the
+ * word is then cleared).  *word (nullable) receives the raw flags. */
+sp_status sp_get_status(sp_cache* cache, void* stream, int32_t* word);
+
+/* Message of the last failing call on this thread ("" if none). */
+const char* sp_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SEGPAGED_H */

@@ -1,0 +1,196 @@
+"""GPU: tcgen05 prefill against the CPU oracle (through the C ABI)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from _gpu_common import compare, f64, gpu_ready, ncores, pol_tuple, to_c_policies
+
+pytestmark = pytest.mark.gpu
+
+G, L, R = W.GLOBAL, W.LOCAL, W.RETRIEVAL
+
+
+def _mk(layers, hq, hkv, d, P, max_seqs, max_len, num_pages, max_batch=8, max_idx=8192,
+        max_tokens=None):
+    from head_aware_paged_gb300 import Config, SegPagedCache
+    cfg = Config(num_layers=layers, num_q_heads=hq, num_kv_heads=hkv, head_dim=d, page_size=P,
+                 max_seqs=max_seqs, max_seq_len=max_len, num_pages=num_pages,
+                 max_idx_per_seq=max_idx, max_tokens=max_tokens or max_len, max_batch=max_batch)
+    return SegPagedCache(cfg)
+
+
+def test_tiny_prefill_then_decode():
+    """Tiny case end to end: 256-row causal prefill, append, 4 decode steps."""
+    gpu_ready()
+    wl = W.WORKLOADS["tiny"]
+    cache = _mk(1, wl.hq, wl.hkv, wl.d, wl.page, 1, 512, 64)
+    pols = W.policies(wl)
+    pt = [pol_tuple(p) for p in pols[0]]
+    cache.set_policy(0, to_c_policies(pols))
+    q, k, v = W.qkv(wl, 256 + 4, 0, 0, device="cuda")
+    out, lse = cache.prefill(0, [0], [0, 256], q[:256].contiguous(), k[:256].contiguous(),
+                             v[:256].contiguous())
+    ref, lref = oracle.attend(f64(q[:256]), f64(k[:256]), f64(v[:256]), np.arange(256), pt, "f64")
+    compare(out, ref, lse, lref, "tiny prefill")
+    cache.append_kv(0, [0], [0, 256], k[:256].contiguous(), v[:256].contiguous())
+    for step in range(4):
+        t = 256 + step
+        cache.append_kv(0, [0], [0, 1], k[t:t + 1].contiguous(), v[t:t + 1].contiguous())
+        o, l_ = cache.decode(0, [0], q[t:t + 1].contiguous())
+        r, lr = oracle.attend(f64(q[t:t + 1]), f64(k[:t + 1]), f64(v[:t + 1]), [t], pt, "f64")
+        compare(o, r, l_, lr, "tiny decode %d" % step)
+    assert cache.status() == 0
+
+
+def test_mistral7b_shape_one_shot():
+    """Mistral-7B-shaped layer: Hq 32 / Hkv 8, d 128, L 8192, P 64, 1 GLOBAL +
+    7 LOCAL(4, 1024); oracle on every 5th row plus the first and last 128."""
+    gpu_ready()
+    wl = W.WORKLOADS["mistral7b_prefill_8k"]
+    Lq = wl.seq_len
+    cache = _mk(1, wl.hq, wl.hkv, wl.d, wl.page, 1, Lq, 400)
+    pols = W.policies(wl)
+    cache.set_policy(0, to_c_policies(pols))
+    q, k, v = W.qkv(wl, Lq, 0, 0, device="cuda")
+    out, lse = cache.prefill(0, [0], [0, Lq], q, k, v)
+    rows = np.unique(np.concatenate([np.arange(0, Lq, 5), np.arange(128), np.arange(Lq - 128, Lq)]))
+    pt = [pol_tuple(p) for p in pols[0]]
+    ref, lref = oracle.attend(f64(q[rows]), f64(k), f64(v), rows, pt, "f64", threads=ncores())
+    compare(out[rows], ref, lse[rows], lref, "mistral one-shot")
+    assert cache.status() == 0
+
+
+def _rand_policies(hkv, max_len, rng, sink_hi=9, win_hi=700, idx_hi=500):
+    row = []
+    for h in range(hkv):
+        kind = h % 3 if hkv >= 3 else int(rng.integers(0, 3))
+        if kind == G:
+            row.append(W.HeadPolicy(G))
+        elif kind == L:
+            row.append(W.HeadPolicy(L, int(rng.integers(0, sink_hi)), int(rng.integers(1, win_hi))))
+        else:
+            idx = np.sort(rng.choice(max_len, int(rng.integers(0, idx_hi)), replace=False))
+            row.append(W.HeadPolicy(R, idx=idx.astype(np.int32)))
+    return row
+
+
+@pytest.mark.parametrize("P,d,hq,hkv", [(64, 128, 16, 4), (16, 64, 8, 4), (128, 128, 12, 3),
+                                        (32, 64, 6, 3)])
+def test_chunked_ragged_prefill_with_history(P, d, hq, hkv):
+    """Several sequences prefilled in ragged chunks (history from pages, the
+    rest from the chunk), mixed classes incl. RETRIEVAL, then decode; every
+    chunk's output against the oracle; chunked equals one-shot."""
+    gpu_ready()
+    rng = np.random.default_rng(P + 3 * d + hq)
+    B, max_len = 3, 1700
+    lens = [1700, 901, 333]
+    cache = _mk(1, hq, hkv, d, P, B, max_len, B * hkv * (max_len // P + 3), max_batch=B)
+    oneshot = _mk(1, hq, hkv, d, P, B, max_len, B * hkv * (max_len // P + 3), max_batch=B)
+    pols, data = [], []
+    for b in range(B):
+        row = _rand_policies(hkv, max_len, rng)
+        pols.append(row)
+        cache.set_policy(b, to_c_policies([row]))
+        oneshot.set_policy(b, to_c_policies([row]))
+        data.append((W.normal((lens[b], hq, d), 100 + b, device="cuda"),
+                     W.normal((lens[b], hkv, d), 200 + b, 0.5, device="cuda"),
+                     W.normal((lens[b], hkv, d), 300 + b, device="cuda")))
+    outs = [torch.zeros(lens[b], hq, d, dtype=torch.bfloat16, device="cuda") for b in range(B)]
+    held = [0] * B
+    chunk_sizes = [1, 77, 128, 129, 300, 511, 64, 2000]
+    step = 0
+    while any(held[b] < lens[b] for b in range(B)):
+        seqs = [b for b in range(B) if held[b] < lens[b]]
+        counts = [min(chunk_sizes[(step + b) % len(chunk_sizes)], lens[b] - held[b]) for b in seqs]
+        cu = [0] + list(np.cumsum(counts))
+        qc = torch.cat([data[b][0][held[b]:held[b] + c] for b, c in zip(seqs, counts)]).contiguous()
+        kc = torch.cat([data[b][1][held[b]:held[b] + c] for b, c in zip(seqs, counts)]).contiguous()
+        vc = torch.cat([data[b][2][held[b]:held[b] + c] for b, c in zip(seqs, counts)]).contiguous()
+        o, lse = cache.prefill(0, seqs, cu, qc, kc, vc)
+        for n, (b, c) in enumerate(zip(seqs, counts)):
+            rows = np.arange(held[b], held[b] + c)
+            pt = [pol_tuple(p) for p in pols[b]]
+            e = held[b] + c
+            ref, lref = oracle.attend(f64(data[b][0][held[b]:e]), f64(data[b][1][:e]),
+                                      f64(data[b][2][:e]), rows, pt, "f64", threads=ncores())
+            compare(o[cu[n]:cu[n + 1]], ref, lse[cu[n]:cu[n + 1]], lref,
+                    "step %d seq %d rows %d..%d" % (step, b, held[b], e))
+            outs[b][held[b]:e] = o[cu[n]:cu[n + 1]]
+        cache.append_kv(0, seqs, cu, kc, vc)
+        for b, c in zip(seqs, counts):
+            held[b] += c
+        step += 1
+    # chunking invariance against a one-shot prefill of the whole sequences
+    cu = [0] + list(np.cumsum(lens))
+    o1, _ = oneshot.prefill(0, list(range(B)), cu, torch.cat([x[0] for x in data]).contiguous(),
+                            torch.cat([x[1] for x in data]).contiguous(),
+                            torch.cat([x[2] for x in data]).contiguous())
+    for b in range(B):
+        diff = (o1[cu[b]:cu[b + 1]].float() - outs[b].float()).abs().max().item()
+        assert diff <= 2e-2, (b, diff)
+    # decode after the chunked prefill
+    for b in range(B):
+        kn = W.normal((1, hkv, d), 400 + b, device="cuda")
+        cache.append_kv(0, [b], [0, 1], kn, kn)
+    qd = W.normal((B, hq, d), 500, device="cuda")
+    od, ld = cache.decode(0, list(range(B)), qd)
+    for b in range(B):
+        kn = W.normal((1, hkv, d), 400 + b, device="cuda")
+        kk = torch.cat([data[b][1], kn])
+        vv = torch.cat([data[b][2], kn])
+        pt = [pol_tuple(p) for p in pols[b]]
+        ref, lref = oracle.attend(f64(qd[b:b + 1]), f64(kk), f64(vv), [lens[b]], pt, "f64")
+        compare(od[b:b + 1], ref, ld[b:b + 1], lref, "decode after chunks, seq %d" % b)
+    assert cache.status() == 0 and oneshot.status() == 0
+
+
+def test_edge_cases():
+    """One-row chunks, rows with no visible key (RETRIEVAL before its first
+    index: O = 0, LSE = -inf), sink larger than a tile, window 1, odd group."""
+    gpu_ready()
+    d, P = 64, 16
+    cache = _mk(1, 3, 3, d, P, 2, 600, 600, max_batch=2)
+    pols = [W.HeadPolicy(R, idx=np.array([50, 51, 300], np.int32)),
+            W.HeadPolicy(L, 150, 1), W.HeadPolicy(L, 0, 1)]
+    cache.set_policy(0, to_c_policies([pols]))
+    n = 400
+    q = W.normal((n, 3, d), 1, device="cuda")
+    k = W.normal((n, 3, d), 2, device="cuda")
+    v = W.normal((n, 3, d), 3, device="cuda")
+    pt = [pol_tuple(p) for p in pols]
+    held = 0
+    for c in (1, 1, 60, 1, 200, 137):
+        o, lse = cache.prefill(0, [0], [0, c], q[held:held + c].contiguous(),
+                               k[held:held + c].contiguous(), v[held:held + c].contiguous())
+        ref, lref = oracle.attend(f64(q[held:held + c]), f64(k[:held + c]), f64(v[:held + c]),
+                                  np.arange(held, held + c), pt, "f64")
+        compare(o, ref, lse, lref, "edge chunk at %d" % held)
+        cache.append_kv(0, [0], [0, c], k[held:held + c].contiguous(), v[held:held + c].contiguous())
+        held += c
+    assert cache.status() == 0
+
+
+def test_llama33_70b_shape_sampled():
+    """Llama-3.3-70B-shaped layer at full size: Hq 64 / Hkv 8, d 128, L 131072,
+    LOCAL(4, 8192) and GLOBAL heads, one-shot causal prefill of one layer in the
+    launch configuration the benchmark uses; the oracle checks 24 sampled rows
+    per query head (first, last, window edges, random)."""
+    gpu_ready()
+    wl = W.WORKLOADS["llama33_70b_prefill_128k"]
+    Lq = wl.seq_len
+    pols_all = W.policies(wl)
+    layer = next(l for l, row in enumerate(pols_all) if any(p.kind == G for p in row))
+    pols = [pols_all[layer]]
+    cache = _mk(1, wl.hq, wl.hkv, wl.d, wl.page, 1, Lq, 8 * (Lq // wl.page + 2))
+    cache.set_policy(0, to_c_policies(pols))
+    q, k, v = W.qkv(wl, Lq, 0, layer, device="cuda")
+    out, lse = cache.prefill(0, [0], [0, Lq], q, k, v)
+    rng = np.random.default_rng(11)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, 8191, 8192, 8195, Lq - 129, Lq - 1],
+                                     rng.integers(0, Lq, 15)]))
+    pt = [pol_tuple(p) for p in pols[0]]
+    ref, lref = oracle.attend(f64(q[rows]), f64(k), f64(v), rows, pt, "f64", threads=ncores())
+    compare(out[rows], ref, lse[rows], lref, "llama-70B-shaped layer %d" % layer)
+    assert cache.status() == 0
