@@ -88,8 +88,13 @@ def test_decode_repeat_is_stable():
         cache.build(b, 0, k, k)
     q = W.normal((4, 32, 128), 3, device="cuda")
     o1, l1 = cache.decode(0, [0, 1, 2, 3], q)
+    o1b, l1b = cache.decode(0, [0, 1, 2, 3], q)
+    # same call, same split partition, fixed merge order: bitwise identical
+    assert torch.equal(o1, o1b) and torch.equal(l1, l1b)
+    # another sequence order splits the pages differently: equal within rounding
     o2, l2 = cache.decode(0, [3, 1, 2, 0], q[[3, 1, 2, 0]].contiguous())
-    assert torch.equal(o1[[3, 1, 2, 0]], o2)
+    assert (o1[[3, 1, 2, 0]].float() - o2.float()).abs().max().item() <= 1e-2
+    assert (l1[[3, 1, 2, 0]] - l2).abs().max().item() <= 1e-4
     assert cache.status() == 0
 
 

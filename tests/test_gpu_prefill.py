@@ -86,8 +86,9 @@ def test_chunked_ragged_prefill_with_history(P, d, hq, hkv):
     rng = np.random.default_rng(P + 3 * d + hq)
     B, max_len = 3, 1700
     lens = [1700, 901, 333]
-    cache = _mk(1, hq, hkv, d, P, B, max_len, B * hkv * (max_len // P + 3), max_batch=B)
-    oneshot = _mk(1, hq, hkv, d, P, B, max_len, B * hkv * (max_len // P + 3), max_batch=B)
+    cache = _mk(1, hq, hkv, d, P, B, max_len + 16, B * hkv * (max_len // P + 3), max_batch=B)
+    oneshot = _mk(1, hq, hkv, d, P, B, max_len, B * hkv * (max_len // P + 3), max_batch=B,
+                  max_tokens=B * max_len)
     pols, data = [], []
     for b in range(B):
         row = _rand_policies(hkv, max_len, rng)

@@ -83,7 +83,7 @@ def test_ragged_appends_match_model(P, d):
     """Several sequences, mixed classes, ragged chunk sizes, release and reuse."""
     gpu_ready()
     rng = np.random.default_rng(P + d)
-    layers, hq, hkv, max_len, npages = 2, 8, 3, 1200, 2000
+    layers, hq, hkv, max_len, npages = 2, 9, 3, 1200, 2000
     cache = _mk(layers, hq, hkv, d, P, 4, max_len, npages)
     model = pm.CacheModel(layers, hkv, P, npages)
     dense = {}
@@ -128,7 +128,7 @@ def test_ragged_appends_match_model(P, d):
 def test_out_of_pages_leaves_state_unchanged():
     gpu_ready()
     from head_aware_paged_gb300 import SegPagedError
-    cache = _mk(1, 4, 1, 64, 16, 2, 4096, 10)
+    cache = _mk(1, 4, 1, 64, 16, 2, 4096, 12)
     cache.set_policy(0, [[(G, 0, 0, None)]])
     k = W.normal((200, 1, 64), 5, device="cuda")
     cache.append_kv(0, [0], [0, 150], k[:150].contiguous(), k[:150].contiguous())
@@ -137,8 +137,8 @@ def test_out_of_pages_leaves_state_unchanged():
         cache.append_kv(0, [0], [0, 50], k[150:].contiguous(), k[150:].contiguous())
     assert ei.value.status == 2
     assert cache.free_pages() == free and cache.seq_len(0, 0) == 150
-    # a LOCAL head's pages stop growing: it fits where GLOBAL did not
-    cache.set_policy(1, [[(L, 4, 16, None)]])
+    # a LOCAL head's pages stop growing: its 2 ring pages fit where GLOBAL did not
+    cache.set_policy(1, [[(L, 0, 8, None)]])
     for _ in range(5):
         cache.append_kv(0, [1], [0, 150], k[:150].contiguous(), k[:150].contiguous())
     assert cache.seq_len(1, 0) == 750
