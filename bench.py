@@ -1,0 +1,611 @@
+"""Benchmark of the head-aware paged attention hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload mistral7b_prefill_8k|llama3_8b_decode_32k|llama33_70b_prefill_128k]
+
+Prints ONE JSON line (rank 0).  Default workload: the Mistral-7B-shaped
+prefill layer (Hq 32 / Hkv 8, d 128, one sequence of 8192 tokens, page 64,
+1 GLOBAL + 7 LOCAL(4, 1024) KV heads).  One step is one pass of the whole
+path over that batch: causal prefill of the 8192-token chunk, the trimmed
+KV write of the chunk (page allocation + scatter), one decode token
+(append + split-KV decode), and the release of the sequence's pages.  The
+head-class policy is set once, offline, before timing.
+
+Metric: visible-pair TFLOP/s (FLOP = 4 d per visible (query, key) pair, for
+the prefill rows and the decode row) for prefill workloads; visible-KV GB/s
+(2 d bytes of K and V per visible key and head) for the decode workload.
+Timing: CUDA events on the launching stream after W warm-up steps; L2 is
+flushed (256 MB write) between steps, outside the timed events.  With
+--gpus N > 1 (torchrun), every rank runs the same workload on its own GPU
+(replicas; the path has no cross-GPU exchange) and the value is the sum of
+the ranks' work over the slowest rank's time.
+
+--impl reference times the CPU oracle (plain fp32 C, all host cores) on a
+bounded sample of the same workload, in the same units.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    QUERY = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 10:
+                continue
+            if self.uuid and parts[1] != self.uuid:
+                continue
+            rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[6 + k] == "Active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------- distributed
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ workloads
+
+class PrefillStep:
+    """Prefill + trimmed KV write + one decode token + release, one sequence."""
+
+    def __init__(self, wl, layer_policies, device="cuda"):
+        import torch
+        from head_aware_paged_gb300 import Config, Policy, SegPagedCache
+        self.wl = wl
+        L = wl.seq_len
+        self.L = L
+        pol = [[Policy(p.kind, p.sink, p.window, None if p.idx is None else p.idx.tolist())
+                for p in layer_policies]]
+        pages = 0
+        for p in layer_policies:
+            pages += (L + 1 + wl.page - 1) // wl.page + 2
+        self.cfg = Config(num_layers=1, num_q_heads=wl.hq, num_kv_heads=wl.hkv, head_dim=wl.d,
+                          page_size=wl.page, max_seqs=1, max_seq_len=L + 64, num_pages=pages,
+                          max_idx_per_seq=max(1, sum(0 if p.idx is None else len(p.idx)
+                                                     for p in layer_policies)),
+                          max_tokens=L, max_batch=1)
+        self.cache = SegPagedCache(self.cfg)
+        self.cache.set_policy(0, pol)
+        self.q, self.k, self.v = W.qkv(wl, L + 1, 0, 0, device=device)
+        self.q1 = self.q[L:].contiguous()
+        self.k1 = self.k[L:].contiguous()
+        self.v1 = self.v[L:].contiguous()
+        self.q, self.k, self.v = (self.q[:L].contiguous(), self.k[:L].contiguous(),
+                                  self.v[:L].contiguous())
+        self.out = torch.empty_like(self.q)
+        self.lse = torch.empty(L, wl.hq, dtype=torch.float32, device=device)
+        self.out1 = torch.empty_like(self.q1)
+        self.lse1 = torch.empty(1, wl.hq, dtype=torch.float32, device=device)
+        pairs = self.cache.count_prefill_pairs(0, 0, 0, L)
+        dec_pairs = self.cache.count_decode_bytes(0, [0], [L]) // (2 * wl.d * 2) * (wl.hq // wl.hkv)
+        self.prefill_flop = 4 * wl.d * pairs
+        self.work = 4 * wl.d * (pairs + dec_pairs)      # FLOP per step
+        self.kernels_per_step = 7                        # prefill, 2x(alloc+scatter), decode, release
+        self.unit = "TFLOP/s"
+
+    def run(self, ev_pf=None):
+        c = self.cache
+        if ev_pf is not None:
+            ev_pf[0].record()
+        c.prefill(0, [0], [0, self.L], self.q, self.k, self.v, self.out, self.lse)
+        if ev_pf is not None:
+            ev_pf[1].record()
+        c.append_kv(0, [0], [0, self.L], self.k, self.v)
+        c.append_kv(0, [0], [0, 1], self.k1, self.v1)
+        c.decode(0, [0], self.q1, self.out1, self.lse1)
+        c.release(0)
+
+    # host-buffer (end-to-end) variant
+    def setup_e2e(self):
+        import torch
+        self.hq_ = self.q.cpu().pin_memory()
+        self.hk_ = self.k.cpu().pin_memory()
+        self.hv_ = self.v.cpu().pin_memory()
+        self.hq1 = self.q1.cpu().pin_memory()
+        self.hk1 = self.k1.cpu().pin_memory()
+        self.hv1 = self.v1.cpu().pin_memory()
+        self.hout = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        self.hout1 = torch.empty(self.out1.shape, dtype=self.out1.dtype).pin_memory()
+        self.hlse = torch.empty(self.lse.shape, dtype=self.lse.dtype).pin_memory()
+        tensors_in = [self.hq_, self.hk_, self.hv_, self.hq1, self.hk1, self.hv1]
+        self.h2d_bytes = sum(t.numel() * t.element_size() for t in tensors_in)
+        self.d2h_bytes = sum(t.numel() * t.element_size() for t in (self.hout, self.hout1, self.hlse))
+
+    def run_e2e(self):
+        self.q.copy_(self.hq_, non_blocking=True)
+        self.k.copy_(self.hk_, non_blocking=True)
+        self.v.copy_(self.hv_, non_blocking=True)
+        self.q1.copy_(self.hq1, non_blocking=True)
+        self.k1.copy_(self.hk1, non_blocking=True)
+        self.v1.copy_(self.hv1, non_blocking=True)
+        self.run()
+        self.hout.copy_(self.out, non_blocking=True)
+        self.hout1.copy_(self.out1, non_blocking=True)
+        self.hlse.copy_(self.lse, non_blocking=True)
+
+    # CPU oracle sample of the same workload: rows spread over the sequence
+    def oracle_sample(self, layer_policies, target_s: float, threads: int):
+        import oracle
+        from oracle import accounting
+        pt = [(p.kind, p.sink, p.window, None if p.idx is None else p.idx.tolist())
+              for p in layer_policies]
+        qf = self.q.float().cpu().numpy()
+        kf = self.k.float().cpu().numpy()
+        vf = self.v.float().cpu().numpy()
+        L = self.L
+        rng = np.random.default_rng(5)
+
+        def run_rows(nrows):
+            rows = np.sort(rng.choice(L, size=nrows, replace=False))
+            t0 = time.perf_counter()
+            oracle.attend(qf[rows], kf, vf, rows, pt, "f32", threads=threads)
+            dt = time.perf_counter() - t0
+            pairs = 0
+            grp = self.wl.hq // self.wl.hkv
+            for p in pt:
+                pairs += grp * int(accounting.vis_count_closed(p[0], p[1], p[2], p[3], rows).sum())
+            return dt, 4 * self.wl.d * pairs, nrows
+
+        dt, fl, n = run_rows(16)
+        n2 = int(min(L, max(16, 16 * target_s / max(dt, 1e-3))))
+        return run_rows(n2), qf, kf, vf, pt
+
+
+class DecodeStep:
+    """Llama-3-8B-shaped decode: per layer, append one token per sequence and
+    decode the batch; one step = all layers."""
+
+    def __init__(self, wl, device="cuda", layers=None):
+        import torch
+        from head_aware_paged_gb300 import Config, Policy, SegPagedCache
+        self.wl = wl
+        self.layers = layers or wl.layers
+        B, n = wl.seqs, wl.seq_len
+        pols = W.policies(wl)[:self.layers]
+        self.pols = pols
+        steps_cap = 256
+        pages = 0
+        for row in pols:
+            for p in row:
+                if p.kind == W.GLOBAL:
+                    pages += B * ((n + steps_cap) // wl.page + 1)
+                else:
+                    pages += B * ((p.sink + wl.page - 1) // wl.page + (p.window + wl.page - 1) // wl.page + 1)
+        self.cfg = Config(num_layers=self.layers, num_q_heads=wl.hq, num_kv_heads=wl.hkv,
+                          head_dim=wl.d, page_size=wl.page, max_seqs=B, max_seq_len=n + steps_cap,
+                          num_pages=pages + 16, max_tokens=max(n, B), max_batch=B)
+        self.cache = SegPagedCache(self.cfg)
+        cp = [[Policy(p.kind, p.sink, p.window) for p in row] for row in pols]
+        for b in range(B):
+            self.cache.set_policy(b, cp)
+        for l in range(self.layers):
+            for b in range(B):
+                k = W.normal((n, wl.hkv, wl.d), W.tensor_seed(0, "k", b, l), device=device)
+                v = W.normal((n, wl.hkv, wl.d), W.tensor_seed(0, "v", b, l), device=device)
+                self.cache.build(b, l, k, v)
+                del k, v
+        torch.cuda.synchronize()
+        self.B, self.n = B, n
+        self.qs = W.normal((B, wl.hq, wl.d), 11, device=device)
+        self.kn = W.normal((B, wl.hkv, wl.d), 12, device=device)
+        self.vn = W.normal((B, wl.hkv, wl.d), 13, device=device)
+        self.out = torch.empty_like(self.qs)
+        self.lse = torch.empty(B, wl.hq, dtype=torch.float32, device=device)
+        self.cu = list(range(B + 1))
+        self.seqs = list(range(B))
+        self.unit = "GB/s"
+        self.kernels_per_step = 3 * self.layers
+        self.t = n      # position of the next token
+
+    def step_bytes(self, t):
+        return sum(self.cache.count_decode_bytes(l, self.seqs, [t] * self.B)
+                   for l in range(self.layers))
+
+    def run(self, ev_pf=None):
+        c = self.cache
+        for l in range(self.layers):
+            c.append_kv(l, self.seqs, self.cu, self.kn, self.vn)
+            if ev_pf is not None and l == 0:
+                ev_pf[0].record()
+            c.decode(l, self.seqs, self.qs, self.out, self.lse)
+            if ev_pf is not None and l == 0:
+                ev_pf[1].record()
+        self.t += 1
+
+
+# ---------------------------------------------------------------- traffic
+
+def load_traffic(kernel: str, workload: str):
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(kernel + "/" + workload)
+        if e and e.get("source_sha") == source_sha():
+            return e.get("bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+def source_sha():
+    import hashlib
+    h = hashlib.sha1()
+    cs = os.path.join(ROOT, "head_aware_paged_gb300", "csrc")
+    for f in sorted(os.listdir(cs)):
+        with open(os.path.join(cs, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+# ---------------------------------------------------------------- main arms
+
+def run_ours(args, ws, rank):
+    import torch
+    from head_aware_paged_gb300 import build as _b
+    if rank == 0:
+        _b.build()
+    barrier(ws)
+    torch.cuda.init()
+    wl = W.WORKLOADS[args.workload]
+    decode = wl.decode_steps > 0 and wl.name.startswith("llama3_8b")
+    if decode:
+        st = DecodeStep(wl)
+    else:
+        layer_pols = W.policies(wl)
+        layer = next((l for l, row in enumerate(layer_pols) if any(p.kind == W.GLOBAL for p in row)), 0)
+        st = PrefillStep(wl, layer_pols[layer])
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup):
+        st.run()
+    torch.cuda.synchronize()
+    assert st.cache.status() == 0
+
+    n_steps = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n_steps)]
+    evk = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n_steps)]
+    work = []
+    kern_work = []
+    props = torch.cuda.get_device_properties(0)
+    uuid = None
+    try:
+        u = str(props.uuid)
+        uuid = u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid if rank == 0 else None)
+    if rank == 0:
+        clocks.start()
+        time.sleep(0.4)
+    barrier(ws)
+    torch.cuda.synchronize()
+    for i in range(n_steps):
+        flush.random_(0, 255) if i == 0 else flush.fill_(i & 0xFF)
+        if decode:
+            work.append(st.step_bytes(st.t))
+            kern_work.append(st.cache.count_decode_bytes(0, st.seqs, [st.t] * st.B))
+        else:
+            work.append(st.work)
+            kern_work.append(st.prefill_flop)
+        ev[i][0].record(stream)
+        st.run(evk[i])
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clk = clocks.stop() if rank == 0 else None
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    kern_ms = [a.elapsed_time(b) for a, b in evk]
+    total_ms = reduce_max(float(sum(step_ms)), ws)
+    assert st.cache.status() == 0
+    scale = 1e-12 if not decode else 1e-9
+    value = ws * sum(work) * scale / (total_ms / 1e3)
+
+    # end-to-end through the same C-ABI calls with host buffers (prefill only)
+    e2e = None
+    if not decode:
+        st.setup_e2e()
+        for _ in range(2):
+            st.run_e2e()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e2e_steps = max(3, min(n_steps, 10))
+        barrier(ws)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            st.run_e2e()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = reduce_max(e0.elapsed_time(e1), ws)
+        e2e = {"value": ws * st.work * e2e_steps * scale / (e2e_ms / 1e3), "unit": st.unit,
+               "h2d_bytes_per_step": st.h2d_bytes, "d2h_bytes_per_step": st.d2h_bytes}
+    else:
+        bytes_in = (st.qs.numel() + st.kn.numel() + st.vn.numel()) * 2 * st.layers
+        bytes_out = (st.out.numel() * 2 + st.lse.numel() * 4) * st.layers
+        hq_ = st.qs.cpu().pin_memory()
+        hk_ = st.kn.cpu().pin_memory()
+        hv_ = st.vn.cpu().pin_memory()
+        ho = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+        hl = torch.empty(st.lse.shape, dtype=st.lse.dtype).pin_memory()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e2e_steps = 3
+        w = 0
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            w += st.step_bytes(st.t)
+            c = st.cache
+            for l in range(st.layers):
+                st.qs.copy_(hq_, non_blocking=True)
+                st.kn.copy_(hk_, non_blocking=True)
+                st.vn.copy_(hv_, non_blocking=True)
+                c.append_kv(l, st.seqs, st.cu, st.kn, st.vn)
+                c.decode(l, st.seqs, st.qs, st.out, st.lse)
+                ho.copy_(st.out, non_blocking=True)
+                hl.copy_(st.lse, non_blocking=True)
+            st.t += 1
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = reduce_max(e0.elapsed_time(e1), ws)
+        e2e = {"value": ws * w * scale / (e2e_ms / 1e3), "unit": st.unit,
+               "h2d_bytes_per_step": bytes_in, "d2h_bytes_per_step": bytes_out}
+
+    if rank != 0:
+        return None
+    peaks, src = load_peaks()
+    kern_avg_ms = float(np.mean(kern_ms))
+    if decode:
+        achieved = float(np.mean(kern_work)) / (kern_avg_ms / 1e3) / 1e9
+        peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": load_traffic("k_decode", wl.name),
+                "kernel": "k_decode", "peak_source": src + " hbm_gbs",
+                "algorithmic_bytes_per_launch": int(np.mean(kern_work)),
+                "avg_launch_ms": kern_avg_ms}
+    else:
+        achieved = st.prefill_flop / (kern_avg_ms / 1e3) / 1e12
+        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": load_traffic("k_prefill", wl.name),
+                "kernel": "k_prefill", "peak_source": src + " bf16_tflops (burst)",
+                "algorithmic_flop_per_launch": st.prefill_flop, "avg_launch_ms": kern_avg_ms}
+
+    cpu = None
+    if ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(st, wl, decode)
+    line = {
+        "metric": "SegPaged prefill TFLOP/s & decode visible-KV GB/s, % of GB300 roofline",
+        "value": value, "unit": st.unit, "n_gpus": ws, "steps": n_steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / n_steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1), pages' shapes)",
+        "config": config_dict(wl, decode, st),
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": st.kernels_per_step * n_steps, "clocks": clk,
+    }
+    return line
+
+
+def config_dict(wl, decode, st):
+    d = {"workload": wl.name, "hq": wl.hq, "hkv": wl.hkv, "head_dim": wl.d, "page_size": wl.page,
+         "l2": "flushed between steps (256 MB write outside the timed events)",
+         "parallelism": "replicas (no cross-GPU exchange on this path)"}
+    if decode:
+        d.update({"layers": st.layers, "batch": wl.seqs, "cached_tokens": wl.seq_len,
+                  "global_units": wl.n_global, "local": [wl.local_sink, wl.local_window],
+                  "step": "all layers: append 1 token/seq + split-KV decode"})
+    else:
+        d.update({"seq_len": wl.seq_len, "global_kv_heads_in_layer": sum(
+            1 for p in W.policies(wl)[0] if p.kind == W.GLOBAL),
+                  "local": [wl.local_sink, wl.local_window],
+                  "step": "prefill + trimmed KV write + 1 decode token + release"})
+    return d
+
+
+def cpu_baseline(st, wl, decode, target_s=12.0):
+    threads = os.cpu_count() or 1
+    if decode:
+        import oracle
+        # layer 0 of two sequences, one decode query each, K/V regenerated on the host
+        seqs = [0, wl.seqs - 1]
+        busy = 0.0
+        nbytes = 0
+        pt = [(p.kind, p.sink, p.window, None) for p in st.pols[0]]
+        qf = st.qs.float().cpu().numpy()
+        t = st.n - 1
+        for b in seqs:
+            k = W.normal((st.n, wl.hkv, wl.d), W.tensor_seed(0, "k", b, 0)).float().numpy()
+            v = W.normal((st.n, wl.hkv, wl.d), W.tensor_seed(0, "v", b, 0)).float().numpy()
+            t1 = time.perf_counter()
+            oracle.attend(qf[b:b + 1], k, v, [t], pt, "f32", threads=threads)
+            busy += time.perf_counter() - t1
+            nbytes += st.cache.count_decode_bytes(0, [b], [t])
+        return {"value": nbytes / busy / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                "sample": "layer 0, sequences 0 and %d, one decode query each over %d cached "
+                          "tokens (fp32 C oracle)" % (wl.seqs - 1, st.n)}
+    (dt, fl, n), *_ = st.oracle_sample(W.policies(wl)[0], target_s, threads)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": "%d of %d query rows (all %d heads), fp32 C oracle" % (n, st.L, wl.hq)}
+
+
+def run_reference(args, ws, rank):
+    """The CPU oracle as the reference arm: each step one bounded sample."""
+    if ws > 1 and rank != 0:
+        return None
+    import oracle
+    from oracle import accounting
+    wl = W.WORKLOADS[args.workload]
+    threads = os.cpu_count() or 1
+    decode = wl.name.startswith("llama3_8b")
+    rng = np.random.default_rng(1)
+    if decode:
+        L = wl.seq_len
+        pol = W.policies(wl)[0]
+        pt = [(p.kind, p.sink, p.window, None) for p in pol]
+        k = W.normal((L, wl.hkv, wl.d), W.tensor_seed(0, "k", 0, 0)).float().numpy()
+        v = W.normal((L, wl.hkv, wl.d), W.tensor_seed(0, "v", 0, 0)).float().numpy()
+        q = W.normal((1, wl.hq, wl.d), 11).float().numpy()
+        nb = sum(int(accounting.vis_count_closed(p[0], p[1], p[2], p[3], np.array([L - 1]))[0])
+                 for p in pt) * 2 * wl.d * 2
+
+        def one():
+            oracle.attend(q, k, v, [L - 1], pt, "f32", threads=threads)
+            return nb
+        unit, scale, sample = "GB/s", 1e-9, "one decode query of one sequence, layer 0, fp32 C oracle"
+    else:
+        L = wl.seq_len
+        pol = W.policies(wl)
+        layer = next((l for l, row in enumerate(pol) if any(p.kind == W.GLOBAL for p in row)), 0)
+        pt = [(p.kind, p.sink, p.window, None) for p in pol[layer]]
+        q, k, v = (t.float().numpy() for t in W.qkv(wl, L, 0, 0))
+        grp = wl.hq // wl.hkv
+        nrows = 48
+
+        def one():
+            rows = np.sort(rng.choice(L, size=nrows, replace=False))
+            oracle.attend(q[rows], k, v, rows, pt, "f32", threads=threads)
+            return 4 * wl.d * sum(grp * int(accounting.vis_count_closed(p[0], p[1], p[2], p[3], rows).sum())
+                                  for p in pt)
+        unit, scale, sample = "TFLOP/s", 1e-12, "48 random query rows (all heads) per step, fp32 C oracle"
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    work = 0
+    for _ in range(args.steps):
+        work += one()
+    dt = time.perf_counter() - t0
+    value = work * scale / dt
+    return {"impl": "reference", "metric": "SegPaged prefill TFLOP/s & decode visible-KV GB/s, % of GB300 roofline",
+            "value": value, "unit": unit, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded N(0,1), pages' shapes)",
+            "config": {"workload": wl.name, "hq": wl.hq, "hkv": wl.hkv, "head_dim": wl.d},
+            "cpu_baseline": {"value": value, "unit": unit, "kind": "oracle", "cores": threads,
+                             "sample": sample},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="mistral7b_prefill_8k",
+                    choices=["mistral7b_prefill_8k", "llama3_8b_decode_32k", "llama33_70b_prefill_128k"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        ws = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        line = run_reference(args, ws, rank)
+    else:
+        ws, rank, _ = dist_setup()
+        line = run_ours(args, ws, rank)
+    if line is not None and rank == 0:
+        print(json.dumps(line), flush=True)
+    if args.impl != "reference" and ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -23,14 +23,16 @@ constexpr int kTileKeys = 128;
 constexpr int kMaxSegs = 5;
 
 struct Seg {
-    int32_t paged;     // 0 = chunk positions, 1 = unit slots in pages
-    int32_t sinkseg;   // LOCAL sink segment (history slots are all visible)
     int64_t start;     // first position (chunk) or first unit slot (paged, page aligned)
-    int64_t len;       // keys (chunk) or slots (paged)
+    int64_t len;       // keys (chunk) or slots (paged); 0 = unused slot
 };
 
+// Segment slots are fixed per class (static indexing keeps a plan in
+// registers):  GLOBAL  0 history pages, 1 chunk;
+//              LOCAL   0 sink pages, 1 sink rows of the chunk, 2 and 3 ring
+//                      pages (the ring may wrap once), 4 window rows of the chunk;
+//              RETRIEVAL 0 history pages, 1 chunk rows from the first index.
 struct Plan {
-    int nseg;
     Seg seg[kMaxSegs];
     int64_t ntiles;
 };
@@ -44,27 +46,26 @@ struct KvTile {
     int64_t start;     // position of key 0 (chunk) or unit slot of key 0 (paged)
 };
 
-SP_HD void plan_push(Plan& pl, int paged, int sinkseg, int64_t start, int64_t len) {
-    if (len <= 0) return;
-    Seg& s = pl.seg[pl.nseg++];
-    s.paged = paged; s.sinkseg = sinkseg; s.start = start; s.len = len;
-    pl.ntiles += (len + kTileKeys - 1) / kTileKeys;
+SP_HD bool seg_paged(int kind, int s) {
+    return kind == kLocal ? (s == 0 || s == 2 || s == 3) : s == 0;
 }
+
+SP_HD int64_t seg_tiles(int64_t len) { return len > 0 ? (len + kTileKeys - 1) / kTileKeys : 0; }
 
 // Segments of one work item.  n_b: tokens the unit already holds (history);
 // rows i_lo .. i_hi (positions, i_lo >= n_b).
 SP_HD Plan make_plan(const UnitPol& u, const int32_t* idx, int64_t n_b, int64_t i_lo,
                      int64_t i_hi, int P) {
     Plan pl;
-    pl.nseg = 0;
-    pl.ntiles = 0;
+    #pragma unroll
+    for (int s = 0; s < kMaxSegs; ++s) { pl.seg[s].start = 0; pl.seg[s].len = 0; }
     if (u.kind == kGlobal) {
-        plan_push(pl, 1, 0, 0, n_b);
-        plan_push(pl, 0, 0, n_b, i_hi + 1 - n_b);
+        pl.seg[0].start = 0;   pl.seg[0].len = n_b;
+        pl.seg[1].start = n_b; pl.seg[1].len = i_hi + 1 - n_b;
     } else if (u.kind == kLocal) {
         const int64_t se = min64(u.sink, i_hi + 1);            // sink positions [0, se)
-        plan_push(pl, 1, 1, 0, min64(se, n_b));
-        if (se > n_b) plan_push(pl, 0, 0, n_b, se - n_b);
+        pl.seg[0].start = 0;   pl.seg[0].len = min64(se, n_b);
+        pl.seg[1].start = n_b; pl.seg[1].len = se - n_b;
         const int64_t wa = max64(u.sink, i_lo - u.window + 1);  // window positions [wa, i_hi]
         if (wa < n_b && wa <= i_hi) {
             const int64_t e = min64(i_hi + 1, n_b);
@@ -73,19 +74,22 @@ SP_HD Plan make_plan(const UnitPol& u, const int32_t* idx, int64_t n_b, int64_t 
             const int64_t fa = qa / P;
             const int64_t np = (qa + (e - wa) - 1) / P - fa + 1;  // ring pages touched (<= ring)
             const int64_t n1 = min64(np, ring - fa);
-            plan_push(pl, 1, 0, base + fa * P, n1 * P);
-            if (np > n1) plan_push(pl, 1, 0, base, (np - n1) * P);
+            pl.seg[2].start = base + fa * P; pl.seg[2].len = n1 * P;
+            pl.seg[3].start = base;          pl.seg[3].len = (np - n1) * P;
         }
         const int64_t ca = max64(wa, n_b);
-        if (ca <= i_hi) plan_push(pl, 0, 0, ca, i_hi + 1 - ca);
+        pl.seg[4].start = ca; pl.seg[4].len = i_hi + 1 - ca;
     } else {
         const int64_t cnt_h = count_below(idx, u.n_idx, n_b);
-        plan_push(pl, 1, 0, 0, cnt_h);
+        pl.seg[0].start = 0; pl.seg[0].len = cnt_h;
         if (cnt_h < u.n_idx && idx[cnt_h] <= i_hi) {
             const int64_t f = idx[cnt_h];
-            plan_push(pl, 0, 0, f, i_hi + 1 - f);
+            pl.seg[1].start = f; pl.seg[1].len = i_hi + 1 - f;
         }
     }
+    pl.ntiles = 0;
+    #pragma unroll
+    for (int s = 0; s < kMaxSegs; ++s) pl.ntiles += seg_tiles(pl.seg[s].len);
     return pl;
 }
 
@@ -94,28 +98,33 @@ SP_HD KvTile plan_tile(const Plan& pl, const UnitPol& u, int64_t t, int64_t i_lo
                        int64_t i_hi) {
     KvTile k;
     k.paged = 0; k.nvalid = 0; k.nkeys = 0; k.full = 0; k.table = 0; k.start = 0;
-    for (int s = 0; s < pl.nseg; ++s) {
-        const Seg& g = pl.seg[s];
-        const int64_t nt = (g.len + kTileKeys - 1) / kTileKeys;
-        if (t >= nt) { t -= nt; continue; }
-        k.paged = g.paged;
-        k.start = g.start + t * kTileKeys;
-        k.nvalid = (int32_t)min64(kTileKeys, g.len - t * kTileKeys);
-        k.nkeys = (k.nvalid + 15) & ~15;
-        const bool exact = k.nkeys == k.nvalid;
-        if (g.paged) {
-            // history: every stored position is < n_b <= i_lo; GLOBAL and
-            // RETRIEVAL slots and LOCAL sink slots are visible to all rows
-            k.full = exact && (u.kind != kLocal || g.sinkseg);
-            k.table = !k.full;
-        } else {
-            const int64_t p0 = k.start, p1 = k.start + k.nvalid - 1;
-            bool full = exact && p1 <= i_lo && u.kind != kRetrieval;
-            if (u.kind == kLocal) full = full && (p1 < u.sink || p0 >= i_hi - u.window + 1);
-            k.full = full;
-            k.table = u.kind == kRetrieval;
+    bool found = false;
+    #pragma unroll
+    for (int s = 0; s < kMaxSegs; ++s) {
+        const int64_t nt = seg_tiles(pl.seg[s].len);
+        if (!found && t < nt) {
+            found = true;
+            const bool paged = seg_paged(u.kind, s);
+            k.paged = paged;
+            k.start = pl.seg[s].start + t * kTileKeys;
+            k.nvalid = (int32_t)min64(kTileKeys, pl.seg[s].len - t * kTileKeys);
+            k.nkeys = (k.nvalid + 15) & ~15;
+            const bool exact = k.nkeys == k.nvalid;
+            if (paged) {
+                // history: every stored position is < n_b <= i_lo; GLOBAL and
+                // RETRIEVAL slots and LOCAL sink slots are visible to all rows
+                k.full = exact && (u.kind != kLocal || s == 0);
+                k.table = !k.full;
+            } else {
+                const int64_t p0 = k.start, p1 = k.start + k.nvalid - 1;
+                bool full = exact && p1 <= i_lo && u.kind != kRetrieval;
+                if (u.kind == kLocal) full = full && (p1 < u.sink || p0 >= i_hi - u.window + 1);
+                k.full = full;
+                k.table = u.kind == kRetrieval;
+            }
+        } else if (!found) {
+            t -= nt;
         }
-        return k;
     }
     return k;
 }
@@ -155,7 +164,8 @@ SP_HD bool key_visible(const KvTile& k, const UnitPol& u, I i, int c, I table_po
 // Work estimate of an item (keys times MMA width), for ordering.
 SP_HD int64_t plan_cost(const Plan& pl) {
     int64_t c = 0;
-    for (int s = 0; s < pl.nseg; ++s) {
+    for (int s = 0; s < kMaxSegs; ++s) {
+        if (pl.seg[s].len <= 0) continue;
         const int64_t full_tiles = pl.seg[s].len / kTileKeys;
         const int64_t rest = pl.seg[s].len - full_tiles * kTileKeys;
         c += full_tiles * kTileKeys + ((rest + 15) & ~15) + (rest > 0 ? 32 : 0) + 32 * full_tiles;

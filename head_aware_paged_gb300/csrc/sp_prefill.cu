@@ -5,16 +5,19 @@
 // KV-cache tutorial section 10.2 (tiling with an online softmax) and 10.4
 // (normalise once at the end); its Hopper FA-3 kernel is prior art only.
 //
-// sm_103a design (one persistent CTA per SM, 12 warps):
-//   warp 0       TMA producer: the work item's Q tiles (128 rows of one or two
+// sm_103a design (one persistent CTA per SM, 12 warps = 3 warpgroups):
+//   warp 8       TMA producer: the work item's Q tiles (128 rows of one or two
 //                query heads of one KV head), then its K/V tiles from the
 //                chunk (2D tensor map) or from cache pages (tensor map over
 //                the page pool), 128-byte swizzled, into a ring of stages.
-//   warp 1       TMEM owner and tcgen05 MMA issuer (one thread): S_t = Q_t K^T
+//   warp 9       TMEM owner and tcgen05 MMA issuer (one thread): S_t = Q_t K^T
 //                into TMEM, later O_t += P_t V with P_t from shared memory.
-//   warps 4-7    softmax + epilogue of query tile 0; warps 8-11 of tile 1.
+//   warps 10-11  idle (the producer/MMA warpgroup gives its registers to the
+//                softmax warpgroups with setmaxnreg).
+//   warps 0-3    softmax + epilogue of query tile 0; warps 4-7 of tile 1.
 //                Each thread owns one query row: it reads its S row from
-//                TMEM, masks (only on tiles that need it, see sp_plan.h),
+//                TMEM (twice, 64 columns at a time: the max, then the
+//                exponentials, so a row never sits in registers whole), masks (only on tiles that need it, see sp_plan.h),
 //                keeps the running max / sum, writes P (bf16) into shared
 //                memory in the MMA operand layout, and rescales its O row in
 //                TMEM only when the max grew by more than 2^8 (lazy rescale).
@@ -24,6 +27,7 @@
 // Every wait is bounded (sp_device.cuh); on a time-out the CTA drains its
 // copies and MMAs, frees TMEM and returns with the status word set.
 #include <algorithm>
+#include <climits>
 #include <cmath>
 #include <memory>
 #include <vector>
@@ -38,7 +42,18 @@ namespace sp {
 
 namespace {
 
-constexpr int kPfThreads = 384;
+constexpr int kPfThreads = 384;        // 3 warpgroups: 2 softmax, 1 producer/MMA
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+// Register split between the warpgroups (setmaxnreg).  The block is launched
+// with kLaunchRegs per thread (384 threads x 168 = 64512 of the SM's 65536);
+// the producer/MMA warpgroup drops to kLowRegs and each softmax warpgroup
+// rises to kHighRegs: 2 x 216 + 72 = 3 x 168, so the increase never waits for
+// registers that do not exist.  The host checks kLaunchRegs before launching.
+constexpr int kLaunchRegs = 168;
+constexpr int kHighRegs = 216;
+constexpr int kLowRegs = 72;
+static_assert(2 * kHighRegs + kLowRegs == 3 * kLaunchRegs, "register split must add up");
 constexpr int kSmemLimit = 232448;     // 227 KB per CTA
 constexpr int kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;   // lazy-rescale threshold (log2 units)
@@ -105,6 +120,23 @@ __device__ __forceinline__ Item load_item(const PrefillParams& p, int n) {
     return m;
 }
 
+// Bits [0, n) set, n clamped to [0, 32].
+__device__ __forceinline__ uint32_t lowmask32(int32_t n) {
+    return n <= 0 ? 0u : n >= 32 ? 0xFFFFFFFFu : ((1u << n) - 1u);
+}
+
+// Load columns [0, min(64, n)) of this thread's S row (n > 0, multiple of
+// 16) from TMEM and wait; columns at or past n are left undefined.
+__device__ __forceinline__ void load_s64(uint32_t taddr, int n, uint32_t (&r)[64]) {
+    if (n >= 64) {
+        tmem_ld64(taddr, r);
+    } else {
+        #pragma unroll
+        for (int g4 = 0; g4 < 4; ++g4)
+            if (g4 * 16 < n) tmem_ld16(taddr + g4 * 16, *reinterpret_cast<uint32_t(*)[16]>(&r[g4 * 16]));
+    }
+}
+
 template <int D, int P>
 __global__ void __launch_bounds__(kPfThreads, 1)
 k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tmQ,
@@ -151,7 +183,7 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tmem_alloc(tmem_holder, kTmemCols);
         tmem_relinquish();
     }
@@ -160,7 +192,9 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp == 0 && lane == 0) {
+    if (warp >= 8) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kLowRegs));
+      if (warp == kProducerWarp && lane == 0) {
         // ------------------------------ producer ------------------------------
         prefetch_tmap(&tmQ); prefetch_tmap(&tmK); prefetch_tmap(&tmV);
         prefetch_tmap(&tmKp); prefetch_tmap(&tmVp);
@@ -208,7 +242,7 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
         for (uint32_t s = 0; s < NS && s < L; ++s)
             mbar_wait(&kv_full[s], ((L - 1 - s) / NS) & 1, nullptr, nullptr);
         if (q_loads > 0) mbar_wait(q_full, (q_loads - 1) & 1, nullptr, nullptr);
-    } else if (warp == 1 && lane == 0) {
+      } else if (warp == kMmaWarp && lane == 0) {
         // ------------------------------ MMA issuer ------------------------------
         const uint32_t q_addr = smem_u32(sQ), p_addr = smem_u32(sP), kv_addr = smem_u32(sKV);
         const uint32_t idesc_pv = idesc_bf16(128, D, true);
@@ -284,11 +318,13 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
         // all MMAs issued by this thread complete before TMEM can be freed
         tc_commit(mma_done);
         mbar_wait(mma_done, 0, nullptr, nullptr);
-    } else if (warp >= 4) {
+      }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kHighRegs));
         // --------------------------- softmax + epilogue ---------------------------
-        const int t = (warp - 4) >> 2;
+        const int t = warp >> 2;
         if (t < nq) {
-            const int r = threadIdx.x - (4 + 4 * t) * 32;             // query row in the tile
+            const int r = threadIdx.x - t * 128;                       // query row in the tile
             const uint32_t lane_off = ((uint32_t)(warp & 3) * 32u) << 16;
             const uint32_t tS = tmem + lane_off + t * 128;
             const uint32_t tO = tmem + lane_off + 256 + t * D;
@@ -324,27 +360,52 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                     }
                     if (!mbar_wait(&s_full[t], k & 1, abort_flag, status)) { ok = false; break; }
                     tc_fence_after();
-                    uint32_t sr[128];
-                    if (kt.nkeys == 128) {
-                        tmem_ld128(tS, sr);
+                    // Visibility bits of this row for columns 0..127.  Chunk tiles
+                    // (affine positions p = start + c): c < nvalid, c <= i - start,
+                    // and for LOCAL c < sink - start or c >= i - window + 1 - start.
+                    // Table tiles: key_visible on the broadcast position table.
+                    uint32_t vm[4];
+                    if (!masked) {
+                        #pragma unroll
+                        for (int w = 0; w < 4; ++w) vm[w] = lowmask32(kt.nkeys - 32 * w);
+                    } else if (!kt.table) {
+                        const int32_t p0 = (int32_t)kt.start;
+                        const int32_t up = min(kt.nvalid, i - p0 + 1);
+                        #pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            uint32_t b = lowmask32(up - 32 * w);
+                            if (it.pol.kind == kLocal)
+                                b &= lowmask32(it.pol.sink - p0 - 32 * w) |
+                                     ~lowmask32(i - it.pol.window + 1 - p0 - 32 * w);
+                            vm[w] = b;
+                        }
                     } else {
                         #pragma unroll
-                        for (int ch = 0; ch < 8; ++ch)
-                            if (ch * 16 < kt.nkeys)
-                                tmem_ld16(tS + ch * 16, *reinterpret_cast<uint32_t(*)[16]>(&sr[ch * 16]));
+                        for (int w = 0; w < 4; ++w) {
+                            uint32_t b = 0;
+                            #pragma unroll
+                            for (int e = 0; e < 32; ++e) {
+                                const int32_t tp = __shfl_sync(0xffffffffu, tpos[w], e);
+                                if (key_visible<int32_t>(kt, it.pol, i, 32 * w + e, tp)) b |= 1u << e;
+                            }
+                            vm[w] = b;
+                        }
                     }
-                    // scale to log2 units, mask, tile max
+                    // pass 1: row maximum (log2 units), 64 columns at a time
                     float tmax = -INFINITY;
                     #pragma unroll
-                    for (int c = 0; c < 128; ++c) {
-                        if (c < kt.nkeys) {
-                            float s = __uint_as_float(sr[c]) * sl2;
-                            if (masked) {
-                                const int32_t tp = kt.table ? __shfl_sync(0xffffffffu, tpos[c >> 5], c & 31) : 0;
-                                if (!key_visible<int32_t>(kt, it.pol, i, c, tp)) s = -INFINITY;
+                    for (int half = 0; half < 2; ++half) {
+                        const int base = half * 64;
+                        if (base < kt.nkeys) {
+                            uint32_t sr[64];
+                            load_s64(tS + base, kt.nkeys - base, sr);
+                            float mx = -INFINITY;
+                            #pragma unroll
+                            for (int e = 0; e < 64; ++e) {
+                                const int c = base + e;
+                                if ((vm[c >> 5] >> (c & 31)) & 1u) mx = fmaxf(mx, __uint_as_float(sr[e]));
                             }
-                            sr[c] = __float_as_uint(s);
-                            tmax = fmaxf(tmax, s);
+                            tmax = fmaxf(tmax, mx * sl2);
                         }
                     }
                     // online softmax with lazy rescale
@@ -359,16 +420,6 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                         resc = true;
                     }
                     const float mb = m == -INFINITY ? 0.f : m;
-                    float rs = 0.f;
-                    #pragma unroll
-                    for (int c = 0; c < 128; ++c) {
-                        if (c < kt.nkeys) {
-                            const float pv = fast_exp2(__uint_as_float(sr[c]) - mb);
-                            rs += pv;
-                            sr[c] = __float_as_uint(pv);
-                        }
-                    }
-                    l = l * alpha + rs;
                     // PV of the previous tile must be done before P is overwritten
                     // and before O is rescaled
                     if (k > 0) {
@@ -387,19 +438,39 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                         }
                         tmem_st_wait();
                     }
-                    // P row -> shared memory, K-major 128-byte-swizzled operand layout
+                    // pass 2: exponentials, row sum, P row -> shared memory in the
+                    // K-major 128-byte-swizzled operand layout
+                    float rs = 0.f;
                     #pragma unroll
-                    for (int c8 = 0; c8 < 16; ++c8) {
-                        if (c8 * 8 < kt.nkeys) {
-                            uint4 v;
-                            v.x = pack_bf16(__uint_as_float(sr[c8 * 8 + 0]), __uint_as_float(sr[c8 * 8 + 1]));
-                            v.y = pack_bf16(__uint_as_float(sr[c8 * 8 + 2]), __uint_as_float(sr[c8 * 8 + 3]));
-                            v.z = pack_bf16(__uint_as_float(sr[c8 * 8 + 4]), __uint_as_float(sr[c8 * 8 + 5]));
-                            v.w = pack_bf16(__uint_as_float(sr[c8 * 8 + 6]), __uint_as_float(sr[c8 * 8 + 7]));
-                            *reinterpret_cast<uint4*>(myP + (c8 >> 3) * S::kHalfBytes +
-                                                      sw128((uint32_t)r, (uint32_t)(c8 & 7))) = v;
+                    for (int half = 0; half < 2; ++half) {
+                        const int base = half * 64;
+                        if (base < kt.nkeys) {
+                            uint32_t sr[64];
+                            load_s64(tS + base, kt.nkeys - base, sr);
+                            #pragma unroll
+                            for (int c8 = 0; c8 < 8; ++c8) {
+                                if (base + c8 * 8 < kt.nkeys) {
+                                    float pv[8];
+                                    #pragma unroll
+                                    for (int e = 0; e < 8; ++e) {
+                                        const int c = base + c8 * 8 + e;
+                                        pv[e] = ((vm[c >> 5] >> (c & 31)) & 1u)
+                                                    ? fast_exp2(fmaf(__uint_as_float(sr[c8 * 8 + e]), sl2, -mb))
+                                                    : 0.f;
+                                        rs += pv[e];
+                                    }
+                                    uint4 v;
+                                    v.x = pack_bf16(pv[0], pv[1]);
+                                    v.y = pack_bf16(pv[2], pv[3]);
+                                    v.z = pack_bf16(pv[4], pv[5]);
+                                    v.w = pack_bf16(pv[6], pv[7]);
+                                    *reinterpret_cast<uint4*>(myP + half * S::kHalfBytes +
+                                                              sw128((uint32_t)r, (uint32_t)c8)) = v;
+                                }
+                            }
                         }
                     }
+                    l = l * alpha + rs;
                     fence_async_smem();
                     tc_fence_before();
                     mbar_arrive(&p_full[t]);
@@ -408,32 +479,35 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                 // epilogue: O / l -> bf16 rows, LSE
                 if (!mbar_wait(&o_full[t], (k - 1) & 1, abort_flag, status)) { ok = false; break; }
                 tc_fence_after();
-                uint32_t orr[D];
-                if constexpr (D == 128) tmem_ld128(tO, orr); else tmem_ld64(tO, orr);
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                #pragma unroll
+                for (int half = 0; half < D / 64; ++half) {
+                    uint32_t orr[64];
+                    tmem_ld64(tO + half * 64, orr);
+                    if (row_ok) {
+                        #pragma unroll
+                        for (int c = 0; c < 64; c += 8) {
+                            uint4 v;
+                            v.x = pack_bf16(__uint_as_float(orr[c + 0]) * inv, __uint_as_float(orr[c + 1]) * inv);
+                            v.y = pack_bf16(__uint_as_float(orr[c + 2]) * inv, __uint_as_float(orr[c + 3]) * inv);
+                            v.z = pack_bf16(__uint_as_float(orr[c + 4]) * inv, __uint_as_float(orr[c + 5]) * inv);
+                            v.w = pack_bf16(__uint_as_float(orr[c + 6]) * inv, __uint_as_float(orr[c + 7]) * inv);
+                            *reinterpret_cast<uint4*>(orow + half * 64 + c) = v;
+                        }
+                    }
+                }
                 tc_fence_before();
                 mbar_arrive(&o_empty[t]);
-                if (row_ok) {
-                    const float inv = l > 0.f ? 1.f / l : 0.f;
-                    #pragma unroll
-                    for (int c = 0; c < D; c += 8) {
-                        uint4 v;
-                        v.x = pack_bf16(__uint_as_float(orr[c + 0]) * inv, __uint_as_float(orr[c + 1]) * inv);
-                        v.y = pack_bf16(__uint_as_float(orr[c + 2]) * inv, __uint_as_float(orr[c + 3]) * inv);
-                        v.z = pack_bf16(__uint_as_float(orr[c + 4]) * inv, __uint_as_float(orr[c + 5]) * inv);
-                        v.w = pack_bf16(__uint_as_float(orr[c + 6]) * inv, __uint_as_float(orr[c + 7]) * inv);
-                        *reinterpret_cast<uint4*>(orow + c) = v;
-                    }
-                    if (p.lse)
-                        p.lse[(it.row_base + r) * g.hq + head] =
-                            l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-                }
+                if (row_ok && p.lse)
+                    p.lse[(it.row_base + r) * g.hq + head] =
+                        l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
             }
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -469,8 +543,13 @@ cudaError_t launch_prefill_t(const sp_cache* c, const PrefillParams& p, int grid
                              const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                              cudaStream_t s) {
     using Sh = PfShape<D>;
-    cudaError_t e = cudaFuncSetAttribute(k_prefill<D, P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Sh::kSmem);
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, k_prefill<D, P>);
+    if (e != cudaSuccess) return e;
+    // The setmaxnreg split assumes exactly kLaunchRegs registers per thread at
+    // launch; anything else could leave an increase waiting forever.
+    if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(k_prefill<D, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmem);
     if (e != cudaSuccess) return e;
     k_prefill<D, P><<<grid, kPfThreads, Sh::kSmem, s>>>(p, tq, tk, tv, c->tm_kpool, c->tm_vpool);
     return cudaGetLastError();
