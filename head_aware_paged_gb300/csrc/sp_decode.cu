@@ -348,25 +348,64 @@ k_decode(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtenso
             }
             asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32));
             if (*flag_last) {
+                // Merge the unit's partials.  Segment sg is CTA c_first + sg
+                // (skipped if its item range is empty).  Stage the (m, l) pairs in
+                // shared memory (the intra-CTA merge buffers are free now), turn
+                // them into weights 2^(m - m*), then sum the weighted partial
+                // outputs with several independent loads in flight per thread.
                 __threadfence();
+                const int nseg = c_last - c_first + 1;
+                float* wts = merge_o;                          // [nseg][group] weights
+                float* mls = merge_o + kConsumerWarps * kMaxGroup * D / 2;  // [nseg][group] l
+                float* mstar = merge_ml;                       // [group] m*, then 1 / l*
+                for (int e = ctid; e < nseg * group; e += kConsumerWarps * 32) {
+                    const int sg = e / group, r = e % group;
+                    const int cc = c_first + sg;
+                    const bool live = (T * cc / G) < (T * (cc + 1) / G);
+                    const int64_t pi = (int64_t)u + cc;
+                    wts[e] = live ? __ldcg(&p.part_ml[(pi * group + r) * 2]) : -INFINITY;
+                    mls[e] = live ? __ldcg(&p.part_ml[(pi * group + r) * 2 + 1]) : 0.f;
+                }
+                asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32));
+                if (ctid < group) {
+                    const int r = ctid;
+                    float mst = -INFINITY;
+                    for (int sg = 0; sg < nseg; ++sg) mst = fmaxf(mst, wts[sg * group + r]);
+                    float lst = 0.f;
+                    for (int sg = 0; sg < nseg; ++sg) {
+                        const float w = fast_exp2(wts[sg * group + r] - mst);
+                        wts[sg * group + r] = w;
+                        lst += w * mls[sg * group + r];
+                    }
+                    mstar[2 * r] = mst;
+                    mstar[2 * r + 1] = lst;
+                }
+                asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32));
                 for (int e = ctid; e < group * D; e += kConsumerWarps * 32) {
                     const int r = e / D, col = e % D;
-                    float mst = -INFINITY;
-                    for (int cc = c_first; cc <= c_last; ++cc) {
-                        if (!((T * cc / G) < (T * (cc + 1) / G))) continue;
-                        mst = fmaxf(mst, __ldcg(&p.part_ml[(((int64_t)u + cc) * group + r) * 2]));
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                    int sg = 0;
+                    for (; sg + 4 <= nseg; sg += 4) {
+                        float v4[4];
+                        #pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float w = wts[(sg + q) * group + r];
+                            const int64_t pi = (int64_t)u + c_first + sg + q;
+                            v4[q] = w != 0.f ? __ldcg(&p.part_o[(pi * group + r) * D + col]) * w : 0.f;
+                        }
+                        #pragma unroll
+                        for (int q = 0; q < 4; ++q) acc[q] += v4[q];
                     }
-                    float lst = 0.f, ost = 0.f;
-                    for (int cc = c_first; cc <= c_last; ++cc) {
-                        if (!((T * cc / G) < (T * (cc + 1) / G))) continue;
-                        const int64_t pi = (int64_t)u + cc;
-                        const float w = fast_exp2(__ldcg(&p.part_ml[(pi * group + r) * 2]) - mst);
-                        lst += w * __ldcg(&p.part_ml[(pi * group + r) * 2 + 1]);
-                        ost += w * __ldcg(&p.part_o[(pi * group + r) * D + col]);
+                    for (; sg < nseg; ++sg) {
+                        const float w = wts[sg * group + r];
+                        const int64_t pi = (int64_t)u + c_first + sg;
+                        if (w != 0.f) acc[0] += w * __ldcg(&p.part_o[(pi * group + r) * D + col]);
                     }
+                    const float ost = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+                    const float lst = mstar[2 * r + 1];
                     const int64_t orow = (int64_t)b * g.hq + h * group + r;
                     p.out[orow * D + col] = __float2bfloat16(ost / lst);
-                    if (col == 0 && p.lse) p.lse[orow] = (mst + __log2f(lst)) * 0.69314718055994531f;
+                    if (col == 0 && p.lse) p.lse[orow] = (mstar[2 * r] + __log2f(lst)) * 0.69314718055994531f;
                 }
                 if (ctid == 0) p.counters[u] = 0;
             }
@@ -388,8 +427,16 @@ cudaError_t launch_decode_t(const sp_cache* c, const DecodeParams& p, int grid, 
 }  // namespace
 
 cudaError_t launch_decode(const sp_cache* c, const DecodeParams& p, cudaStream_t s) {
+    // Persistent grid, but at least kMinItemsPerCta pages per CTA: a small batch
+    // then spreads one head over a few CTAs instead of dozens (fewer partials
+    // to merge).
+    constexpr int64_t kMinItemsPerCta = 8;
     int grid = c->decode_ctas;
-    if (p.total_items < grid) grid = (int)(p.total_items > 0 ? p.total_items : 1);
+    const int64_t want = (p.total_items + kMinItemsPerCta - 1) / kMinItemsPerCta;
+    if (want < grid) grid = (int)(want > 0 ? want : 1);
+    // the merge stages up to grid x group (m, l) pairs in half of the merge buffer
+    const int merge_cap = kConsumerWarps * kMaxGroup * c->geo.d / 2 / c->geo.group;
+    if (grid > merge_cap) grid = merge_cap;
     const int D = c->geo.d, P = c->geo.page;
 #define SP_DEC(DD, PP) if (D == DD && P == PP) return launch_decode_t<DD, PP>(c, p, grid, s);
     SP_DEC(64, 16) SP_DEC(64, 32) SP_DEC(64, 64) SP_DEC(64, 128)

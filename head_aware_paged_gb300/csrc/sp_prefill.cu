@@ -23,13 +23,16 @@
 //                TMEM only when the max grew by more than 2^8 (lazy rescale).
 //   The two query tiles share every K/V tile and ping-pong on the tensor core:
 //   while one softmax group works, the MMA warp runs the other's PV and next QK.
-// Work items are cost-sorted on the host and dealt round-robin to the CTAs.
+// Work items are assigned to CTAs on the host, longest first, each to the
+// CTA with the least work so far (greedy LPT), so no SM idles at the tail.
 // Every wait is bounded (sp_device.cuh); on a time-out the CTA drains its
 // copies and MMAs, frees TMEM and returns with the status word set.
 #include <algorithm>
 #include <climits>
 #include <cmath>
 #include <memory>
+#include <queue>
+#include <utility>
 #include <vector>
 
 #include "sp_device.cuh"
@@ -65,7 +68,8 @@ struct PrefillParams {
     int32_t nq;                  // query tiles per item: 2 (head pairs) or 1
     int32_t n_items;
     float scale_log2;            // log2(e) / sqrt(d)
-    const int4* items;           // {b, kv head, head pair, row block}
+    const int4* items;           // {b, kv head, head pair, row block}, grouped by CTA
+    const int32_t* cta_off;      // items of CTA c: [cta_off[c], cta_off[c+1])
     __nv_bfloat16* out;
     float* lse;
     int32_t seq[kMaxCallSeqs];
@@ -200,7 +204,7 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
         prefetch_tmap(&tmKp); prefetch_tmap(&tmVp);
         uint32_t q_loads = 0, L = 0;
         bool ok = true;
-        for (int n = cta; n < p.n_items && ok; n += G) {
+        for (int n = p.cta_off[cta]; n < p.cta_off[cta + 1] && ok; ++n) {
             const Item it = load_item(p, n);
             const Plan pl = make_plan(it.pol, it.idx, it.n_b, it.i_lo, it.i_hi, P);
             if (pl.ntiles == 0) continue;
@@ -268,7 +272,7 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
         uint32_t q_uses = 0, L = 0, e = 0;
         uint32_t tiles_t[2] = {0, 0};
         bool ok = true;
-        for (int n = cta; n < p.n_items && ok; n += G) {
+        for (int n = p.cta_off[cta]; n < p.cta_off[cta + 1] && ok; ++n) {
             const Item it = load_item(p, n);
             const Plan pl = make_plan(it.pol, it.idx, it.n_b, it.i_lo, it.i_hi, P);
             const int64_t nt = pl.ntiles;
@@ -332,7 +336,7 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
             const float sl2 = p.scale_log2;
             uint32_t k = 0;
             bool ok = true;
-            for (int n = cta; n < p.n_items && ok; n += G) {
+            for (int n = p.cta_off[cta]; n < p.cta_off[cta + 1] && ok; ++n) {
                 const Item it = load_item(p, n);
                 const Plan pl = make_plan(it.pol, it.idx, it.n_b, it.i_lo, it.i_hi, P);
                 const int head = it.h0 + t;
@@ -399,13 +403,19 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                         if (base < kt.nkeys) {
                             uint32_t sr[64];
                             load_s64(tS + base, kt.nkeys - base, sr);
-                            float mx = -INFINITY;
+                            // eight independent maxima, then a tree: short dependency chains
+                            float mx[8];
+                            #pragma unroll
+                            for (int a = 0; a < 8; ++a) mx[a] = -INFINITY;
                             #pragma unroll
                             for (int e = 0; e < 64; ++e) {
                                 const int c = base + e;
-                                if ((vm[c >> 5] >> (c & 31)) & 1u) mx = fmaxf(mx, __uint_as_float(sr[e]));
+                                if ((vm[c >> 5] >> (c & 31)) & 1u) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(sr[e]));
                             }
-                            tmax = fmaxf(tmax, mx * sl2);
+                            #pragma unroll
+                            for (int a = 0; a < 4; ++a) mx[a] = fmaxf(mx[a], mx[a + 4]);
+                            mx[0] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                            tmax = fmaxf(tmax, mx[0] * sl2);
                         }
                     }
                     // online softmax with lazy rescale
@@ -440,7 +450,7 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                     }
                     // pass 2: exponentials, row sum, P row -> shared memory in the
                     // K-major 128-byte-swizzled operand layout
-                    float rs = 0.f;
+                    float rsum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
                     #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         const int base = half * 64;
@@ -457,7 +467,7 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                                         pv[e] = ((vm[c >> 5] >> (c & 31)) & 1u)
                                                     ? fast_exp2(fmaf(__uint_as_float(sr[c8 * 8 + e]), sl2, -mb))
                                                     : 0.f;
-                                        rs += pv[e];
+                                        rsum[e] += pv[e];
                                     }
                                     uint4 v;
                                     v.x = pack_bf16(pv[0], pv[1]);
@@ -470,6 +480,8 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                             }
                         }
                     }
+                    const float rs = ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3])) +
+                                     ((rsum[4] + rsum[5]) + (rsum[6] + rsum[7]));
                     l = l * alpha + rs;
                     fence_async_smem();
                     tc_fence_before();
@@ -558,7 +570,8 @@ cudaError_t launch_prefill_t(const sp_cache* c, const PrefillParams& p, int grid
 }  // namespace
 
 int64_t prefill_max_tiles(const sp_config* c) {
-    return ((int64_t)c->max_tokens / 128 + c->max_batch + 1) * c->num_q_heads;
+    // work items plus room for the per-CTA offsets behind them
+    return ((int64_t)c->max_tokens / 128 + c->max_batch + 1) * c->num_q_heads + 512;
 }
 
 sp_status prefill_impl(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32_t n_seqs,
@@ -602,15 +615,41 @@ sp_status prefill_impl(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32
             }
         }
     }
-    if ((int64_t)cands.size() > c->ws.max_tiles)
+    if ((int64_t)cands.size() + (c->num_sms + 4) / 4 > c->ws.max_tiles)
         return fail(SP_ERR_UNSUPPORTED, "prefill work list larger than the workspace");
     std::stable_sort(cands.begin(), cands.end(),
                      [](const Cand& a, const Cand& b2) { return a.cost > b2.cost; });
-    std::vector<int4> items(cands.size());
-    for (size_t n = 0; n < cands.size(); ++n) items[n] = cands[n].item;
+    // Greedy longest-processing-time assignment: each item, longest first,
+    // goes to the CTA with the least work so far.
+    const int grid = (int)std::min<int64_t>(c->num_sms, (int64_t)cands.size());
+    std::vector<int64_t> load(grid, 0);
+    std::vector<std::vector<int4>> per(grid);
+    {
+        typedef std::pair<int64_t, int> LoadCta;
+        std::priority_queue<LoadCta, std::vector<LoadCta>, std::greater<LoadCta>> heap;
+        for (int g2 = 0; g2 < grid; ++g2) heap.push(LoadCta(0, g2));
+        for (const Cand& cd : cands) {
+            LoadCta top = heap.top();
+            heap.pop();
+            per[top.second].push_back(cd.item);
+            top.first += cd.cost;
+            heap.push(top);
+        }
+    }
+    // one upload: the items grouped by CTA, then the CTA offsets
+    const size_t n_items = cands.size();
+    std::vector<int4> buf(n_items + (grid + 1 + 3) / 4);
+    int32_t* off = reinterpret_cast<int32_t*>(buf.data() + n_items);
+    size_t pos = 0;
+    for (int g2 = 0; g2 < grid; ++g2) {
+        off[g2] = (int32_t)pos;
+        for (const int4& it : per[g2]) buf[pos++] = it;
+    }
+    off[grid] = (int32_t)pos;
     p.items = c->ws.tiles;
-    p.n_items = (int32_t)items.size();
-    cudaError_t e = cudaMemcpyAsync(c->ws.tiles, items.data(), items.size() * sizeof(int4),
+    p.cta_off = reinterpret_cast<const int32_t*>(c->ws.tiles + n_items);
+    p.n_items = (int32_t)n_items;
+    cudaError_t e = cudaMemcpyAsync(c->ws.tiles, buf.data(), buf.size() * sizeof(int4),
                                     cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess) return cuda_fail(e, "prefill work list upload");
     CUtensorMap tq, tk, tv;
@@ -623,7 +662,6 @@ sp_status prefill_impl(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32
         !encode_tmap_2d(&tv, v, (uint64_t)c->cfg.num_kv_heads * D, T,
                         (uint64_t)c->cfg.num_kv_heads * D * 2, 64, 128, true, &err))
         return fail(SP_ERR_CUDA, err);
-    const int grid = (int)std::min<int64_t>(c->num_sms, (int64_t)items.size());
 #define SP_PF(DD, PP) \
     if (D == DD && P == PP) e = launch_prefill_t<DD, PP>(c, p, grid, tq, tk, tv, stream); else
     SP_PF(64, 16) SP_PF(64, 32) SP_PF(64, 64) SP_PF(64, 128)
