@@ -132,6 +132,17 @@ def sp_attention_decode(handle, layer: int, seq_ids: Sequence[int], q: torch.Ten
                                      _ptr(out), _ptr(lse), _stream(stream)))
 
 
+def sp_attention_decode_static_scratch(handle, layer: int, seq_ids: Sequence[int],
+                                       q: torch.Tensor, out: torch.Tensor,
+                                       lse: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Decode whose split scratch is the library's built-in device array, for
+    callers that cannot allocate device memory when they decode (see the C
+    header for the 4 MiB limit and the sharing rules)."""
+    check(load().sp_attention_decode_static_scratch(handle, layer, i32_array(seq_ids),
+                                                    len(seq_ids), _ptr(q), _ptr(out), _ptr(lse),
+                                                    _stream(stream)))
+
+
 def sp_release_seq(handle, seq: int, stream=None) -> None:
     check(load().sp_release_seq(handle, seq, _stream(stream)))
 

@@ -157,6 +157,32 @@ sp_status sp_attention_decode(sp_cache* cache, int32_t layer,
                               const int32_t* seq_ids, int32_t n_seqs,
                               const void* q, void* out, float* lse, void* stream);
 
+/* Decode without any device allocation by the caller for scratch: the same
+ * computation as sp_attention_decode, but the split-KV scratch (partial
+ * outputs, their max / sum and the merge tickets) lives in a fixed 4 MiB
+ * device array compiled into this library instead of the cache's workspace.
+ * (The paper has no counterpart; this entry point is for callers that cannot
+ * allocate device memory when they decode: a plain C host without a device
+ * allocator, or a serving loop that must not call cudaMalloc mid-step because
+ * it can synchronise the device or is forbidden after start-up.)
+ *   - The caller still passes the cache, q, out and lse, as for
+ *     sp_attention_decode.
+ *   - Limit: (n_seqs * num_kv_heads + SM count) * group * (head_dim + 2) * 4
+ *     bytes plus the tickets must fit in 4 MiB; larger calls return
+ *     SP_ERR_UNSUPPORTED before any launch (use sp_attention_decode).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.  The current device must be the cache's.
+ *   - Every call shares the one array; the tickets are cleared at the start of
+ *     each call.  Calls that overlap on the GPU (other streams, other caches)
+ *     race on the array and must not be issued concurrently.
+ *   - Every GPU that loads the library holds the array until the process
+ *     exits. */
+sp_status sp_attention_decode_static_scratch(sp_cache* cache, int32_t layer,
+                                             const int32_t* seq_ids, int32_t n_seqs,
+                                             const void* q, void* out, float* lse,
+                                             void* stream);
+
 /* Return every page of `seq` (all layers) to the free stack and empty it; the
  * policy stays set. */
 sp_status sp_release_seq(sp_cache* cache, int32_t seq, void* stream);
