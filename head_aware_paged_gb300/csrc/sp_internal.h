@@ -9,7 +9,7 @@
 #include <string>
 #include <vector>
 
-#include "../../include/segpaged.h"
+#include "segpaged.h"
 #include "sp_rules.h"
 
 namespace sp {

@@ -129,6 +129,65 @@ SP_HD KvTile plan_tile(const Plan& pl, const UnitPol& u, int64_t t, int64_t i_lo
     return k;
 }
 
+// Incremental walk over a plan's tiles (tile t+1 from tile t without
+// re-scanning the segments).  Positions and slots fit in 32 bits.
+struct TileCursor {
+    int32_t s;        // current segment (kMaxSegs = done)
+    int32_t t_in;     // tile within the segment
+    int32_t nt_s;     // tiles in the segment
+    int32_t start;    // segment start
+    int32_t len;      // segment length
+};
+
+SP_HD void cursor_load(const Plan& pl, TileCursor& c) {
+    // first non-empty segment at or after c.s (static indexing only)
+    int32_t s = kMaxSegs, start = 0, len = 0;
+    #pragma unroll
+    for (int q = kMaxSegs - 1; q >= 0; --q)
+        if (q >= c.s && pl.seg[q].len > 0) { s = q; start = (int32_t)pl.seg[q].start; len = (int32_t)pl.seg[q].len; }
+    c.s = s;
+    c.start = start;
+    c.len = len;
+    c.t_in = 0;
+    c.nt_s = (len + kTileKeys - 1) / kTileKeys;
+}
+
+SP_HD TileCursor cursor_begin(const Plan& pl) {
+    TileCursor c;
+    c.s = 0;
+    cursor_load(pl, c);
+    return c;
+}
+
+SP_HD void cursor_next(const Plan& pl, TileCursor& c) {
+    if (++c.t_in < c.nt_s) return;
+    c.s += 1;
+    cursor_load(pl, c);
+}
+
+// The tile under the cursor (same result as plan_tile for that index).
+SP_HD KvTile cursor_tile(const TileCursor& c, const UnitPol& u, int32_t i_lo, int32_t i_hi) {
+    KvTile k;
+    const bool paged = seg_paged(u.kind, c.s);
+    k.paged = paged;
+    k.start = (int64_t)c.start + (int64_t)c.t_in * kTileKeys;
+    const int32_t rest = c.len - c.t_in * kTileKeys;
+    k.nvalid = rest < kTileKeys ? rest : kTileKeys;
+    k.nkeys = (k.nvalid + 15) & ~15;
+    const bool exact = k.nkeys == k.nvalid;
+    if (paged) {
+        k.full = exact && (u.kind != kLocal || c.s == 0);
+        k.table = !k.full;
+    } else {
+        const int32_t p0 = (int32_t)k.start, p1 = p0 + k.nvalid - 1;
+        bool full = exact && p1 <= i_lo && u.kind != kRetrieval;
+        if (u.kind == kLocal) full = full && (p1 < u.sink || p0 >= i_hi - u.window + 1);
+        k.full = full;
+        k.table = u.kind == kRetrieval;
+    }
+    return k;
+}
+
 // Position of key c of a tile, as the mask sees it (-1 = never visible).
 SP_HD int64_t tile_key_position(const KvTile& k, const UnitPol& u, const int32_t* idx,
                                 int64_t n_b, int c, int P) {

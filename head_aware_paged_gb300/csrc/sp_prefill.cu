@@ -16,8 +16,8 @@
 //                softmax warpgroups with setmaxnreg).
 //   warps 0-3    softmax + epilogue of query tile 0; warps 4-7 of tile 1.
 //                Each thread owns one query row: it reads its S row from
-//                TMEM (twice, 64 columns at a time: the max, then the
-//                exponentials, so a row never sits in registers whole), masks (only on tiles that need it, see sp_plan.h),
+//                TMEM into registers, masks (only on tiles that need it, see
+//                sp_plan.h),
 //                keeps the running max / sum, writes P (bf16) into shared
 //                memory in the MMA operand layout, and rescales its O row in
 //                TMEM only when the max grew by more than 2^8 (lazy rescale).
@@ -51,15 +51,16 @@ constexpr int kMmaWarp = 9;
 // Register split between the warpgroups (setmaxnreg).  The block is launched
 // with kLaunchRegs per thread (384 threads x 168 = 64512 of the SM's 65536);
 // the producer/MMA warpgroup drops to kLowRegs and each softmax warpgroup
-// rises to kHighRegs: 2 x 216 + 72 = 3 x 168, so the increase never waits for
+// rises to kHighRegs: 2 x 208 + 88 = 3 x 168, so the increase never waits for
 // registers that do not exist.  The host checks kLaunchRegs before launching.
 constexpr int kLaunchRegs = 168;
-constexpr int kHighRegs = 216;
-constexpr int kLowRegs = 72;
+constexpr int kHighRegs = 208;
+constexpr int kLowRegs = 88;
 static_assert(2 * kHighRegs + kLowRegs == 3 * kLaunchRegs, "register split must add up");
 constexpr int kSmemLimit = 232448;     // 227 KB per CTA
 constexpr int kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;   // lazy-rescale threshold (log2 units)
+constexpr int kPrefetchTiles = 3;      // K/V tiles brought into L2 ahead of their loads
 
 struct PrefillParams {
     Meta meta;
@@ -124,6 +125,39 @@ __device__ __forceinline__ Item load_item(const PrefillParams& p, int n) {
     return m;
 }
 
+// Packed fp32x2 helpers (sm_100 and later): two lanes of fp32 in one 64-bit
+// register, one instruction per pair.
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ uint64_t pack_u32x2(uint32_t lo, uint32_t hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ __forceinline__ void unpack_f32x2(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+// max(a, b, c) in one instruction (three-input max.f32, sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // Bits [0, n) set, n clamped to [0, 32].
 __device__ __forceinline__ uint32_t lowmask32(int32_t n) {
     return n <= 0 ? 0u : n >= 32 ? 0xFFFFFFFFu : ((1u << n) - 1u);
@@ -179,9 +213,9 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
         for (int s = 0; s < NS; ++s) { mbar_init(&kv_full[s], 1); mbar_init(&kv_empty[s], 1); }
         for (int t = 0; t < 2; ++t) {
             mbar_init(&s_full[t], 1);
-            mbar_init(&p_full[t], 128);
+            mbar_init(&p_full[t], 4);          // one arrival per softmax warp
             mbar_init(&o_full[t], 1);
-            mbar_init(&o_empty[t], 128);
+            mbar_init(&o_empty[t], 4);
         }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
@@ -215,8 +249,49 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                     tma_load_2d(sQ + t * S::kQBytes + hf * S::kHalfBytes, &tmQ, q_full,
                                 (it.h0 + t) * D + hf * 64, (int32_t)it.row_base);
             ++q_loads;
+            // L2 prefetch: the next item's Q now, and K/V tiles kPrefetchTiles
+            // ahead of their loads (HBM latency is longer than the stage ring
+            // can cover on its own)
+            if (n + 1 < p.cta_off[cta + 1]) {
+                const Item nx = load_item(p, n + 1);
+                for (int t = 0; t < nq; ++t)
+                    for (int hf = 0; hf < S::kHalves; ++hf)
+                        tma_prefetch_2d(&tmQ, (nx.h0 + t) * D + hf * 64, (int32_t)nx.row_base);
+            }
+            auto prefetch_tile = [&](const KvTile& pk) {
+                if (!pk.paged) {
+                    const int32_t y = (int32_t)(it.key_row0 + (pk.start - it.n_b));
+                    for (int hf = 0; hf < S::kHalves; ++hf) {
+                        tma_prefetch_2d(&tmK, it.kvh * D + hf * 64, y);
+                        tma_prefetch_2d(&tmV, it.kvh * D + hf * 64, y);
+                    }
+                } else {
+                    const int np = (pk.nkeys + P - 1) / P;
+                    for (int pg = 0; pg < np; ++pg) {
+                        const int32_t phys = it.ptab[pk.start / P + pg];
+                        if (phys < 0 || phys >= g.num_pages) continue;
+                        for (int hf = 0; hf < S::kHalves; ++hf) {
+                            tma_prefetch_2d(&tmKp, hf * 64, phys * P);
+                            tma_prefetch_2d(&tmVp, hf * 64, phys * P);
+                        }
+                    }
+                }
+            };
+            const int32_t ilo32 = (int32_t)it.i_lo, ihi32 = (int32_t)it.i_hi;
+            TileCursor cur = cursor_begin(pl), pre = cursor_begin(pl);
+            int64_t pj = 0;
+            for (; pj < pl.ntiles && pj < kPrefetchTiles; ++pj) {
+                prefetch_tile(cursor_tile(pre, it.pol, ilo32, ihi32));
+                cursor_next(pl, pre);
+            }
             for (int64_t j = 0; j < pl.ntiles && ok; ++j) {
-                const KvTile kt = plan_tile(pl, it.pol, j, it.i_lo, it.i_hi);
+                const KvTile kt = cursor_tile(cur, it.pol, ilo32, ihi32);
+                cursor_next(pl, cur);
+                if (pj < pl.ntiles) {
+                    prefetch_tile(cursor_tile(pre, it.pol, ilo32, ihi32));
+                    cursor_next(pl, pre);
+                    ++pj;
+                }
                 for (int kv = 0; kv < 2; ++kv) {
                     const uint32_t st = L % NS, rd = L / NS;
                     if (rd > 0 && !mbar_wait(&kv_empty[st], (rd - 1) & 1, abort_flag, status)) { ok = false; break; }
@@ -250,23 +325,43 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
         // ------------------------------ MMA issuer ------------------------------
         const uint32_t q_addr = smem_u32(sQ), p_addr = smem_u32(sP), kv_addr = smem_u32(sKV);
         const uint32_t idesc_pv = idesc_bf16(128, D, true);
+        // Descriptors are built once as 32-bit halves; stepping through a tile
+        // only adds the byte offset >> 4 to the low half's start-address field
+        // (no carry: every tile lies inside the 256 KB shared window).
+        const uint64_t dq0 = sdesc_sw128(q_addr, 16, 1024);
+        const uint64_t dp0 = sdesc_sw128(p_addr, 16, 1024);
+        const uint64_t dk0 = sdesc_sw128(kv_addr, 16, 1024);
+        const uint64_t dv0 = sdesc_sw128(kv_addr, S::kHalfBytes, 1024);
+        const uint32_t q_lo = (uint32_t)dq0, p_lo = (uint32_t)dp0, k_lo = (uint32_t)dk0,
+                       v_lo = (uint32_t)dv0;
+        const uint32_t kmaj_hi = (uint32_t)(dq0 >> 32), v_hi = (uint32_t)(dv0 >> 32);
         auto issue_qk = [&](int t, uint32_t st, int nkeys) {
             const uint32_t idesc = idesc_bf16(128, nkeys, false);
+            const uint32_t a0 = q_lo + ((t * S::kQBytes) >> 4);
+            const uint32_t b0 = k_lo + ((st * S::kKVBytes) >> 4);
+            const uint32_t d = tmem + t * 128;
+            tc_mma_first(d, a0, kmaj_hi, b0, kmaj_hi, idesc);
             #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                const uint32_t off = (ks >> 2) * S::kHalfBytes + (ks & 3) * 32;
-                const uint64_t a = sdesc_sw128(q_addr + t * S::kQBytes + off, 16, 1024);
-                const uint64_t b = sdesc_sw128(kv_addr + st * S::kKVBytes + off, 16, 1024);
-                tc_mma(tmem + t * 128, a, b, idesc, ks > 0 ? 1u : 0u);
+            for (int ks = 1; ks < D / 16; ++ks) {
+                const uint32_t off = ((ks >> 2) * S::kHalfBytes + (ks & 3) * 32) >> 4;
+                tc_mma_acc(d, a0 + off, kmaj_hi, b0 + off, kmaj_hi, idesc);
             }
         };
         auto issue_pv = [&](int t, uint32_t st, int nkeys, bool acc) {
-            for (int ks = 0; ks < nkeys / 16; ++ks) {
-                const uint64_t a = sdesc_sw128(p_addr + t * S::kPBytes + (ks >> 2) * S::kHalfBytes +
-                                               (ks & 3) * 32, 16, 1024);
-                const uint64_t b = sdesc_sw128(kv_addr + st * S::kKVBytes + ks * 2048,
-                                               S::kHalfBytes, 1024);
-                tc_mma(tmem + 256 + t * D, a, b, idesc_pv, (acc || ks > 0) ? 1u : 0u);
+            const uint32_t a0 = p_lo + ((t * S::kPBytes) >> 4);
+            const uint32_t b0 = v_lo + ((st * S::kKVBytes) >> 4);
+            const uint32_t d = tmem + 256 + t * D;
+            if (acc) tc_mma_acc(d, a0, kmaj_hi, b0, v_hi, idesc_pv);
+            else tc_mma_first(d, a0, kmaj_hi, b0, v_hi, idesc_pv);
+            if (nkeys == 128) {
+                #pragma unroll
+                for (int ks = 1; ks < 8; ++ks)
+                    tc_mma_acc(d, a0 + (((ks >> 2) * S::kHalfBytes + (ks & 3) * 32) >> 4), kmaj_hi,
+                               b0 + ((ks * 2048) >> 4), v_hi, idesc_pv);
+            } else {
+                for (int ks = 1; ks * 16 < nkeys; ++ks)
+                    tc_mma_acc(d, a0 + (((ks >> 2) * S::kHalfBytes + (ks & 3) * 32) >> 4), kmaj_hi,
+                               b0 + ((ks * 2048) >> 4), v_hi, idesc_pv);
             }
         };
         uint32_t q_uses = 0, L = 0, e = 0;
@@ -279,7 +374,10 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
             if (nt == 0) continue;
             if (!mbar_wait(q_full, q_uses & 1, abort_flag, status)) { ok = false; break; }
             ++q_uses;
-            KvTile kt = plan_tile(pl, it.pol, 0, it.i_lo, it.i_hi);
+            const int32_t ilo32 = (int32_t)it.i_lo, ihi32 = (int32_t)it.i_hi;
+            TileCursor cur = cursor_begin(pl);
+            KvTile kt = cursor_tile(cur, it.pol, ilo32, ihi32);
+            cursor_next(pl, cur);
             uint32_t stK = L % NS;
             if (!mbar_wait(&kv_full[stK], (L / NS) & 1, abort_flag, status)) { ok = false; break; }
             ++L;
@@ -294,7 +392,8 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                 KvTile kn = kt;
                 uint32_t stK2 = 0;
                 if (j + 1 < nt) {
-                    kn = plan_tile(pl, it.pol, j + 1, it.i_lo, it.i_hi);
+                    kn = cursor_tile(cur, it.pol, ilo32, ihi32);
+                    cursor_next(pl, cur);
                     stK2 = L % NS;
                     if (!mbar_wait(&kv_full[stK2], (L / NS) & 1, abort_flag, status)) { ok = false; break; }
                     ++L;
@@ -352,8 +451,10 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                     continue;
                 }
                 float m = -INFINITY, l = 0.f;
+                TileCursor cur = cursor_begin(pl);
                 for (int64_t j = 0; j < pl.ntiles; ++j, ++k) {
-                    const KvTile kt = plan_tile(pl, it.pol, j, it.i_lo, it.i_hi);
+                    const KvTile kt = cursor_tile(cur, it.pol, (int32_t)it.i_lo, (int32_t)it.i_hi);
+                    cursor_next(pl, cur);
                     const bool masked = !kt.full;
                     int32_t tpos[4] = {-1, -1, -1, -1};
                     if (masked && kt.table) {
@@ -395,28 +496,37 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                             vm[w] = b;
                         }
                     }
-                    // pass 1: row maximum (log2 units), 64 columns at a time
-                    float tmax = -INFINITY;
-                    #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        const int base = half * 64;
-                        if (base < kt.nkeys) {
-                            uint32_t sr[64];
-                            load_s64(tS + base, kt.nkeys - base, sr);
-                            // eight independent maxima, then a tree: short dependency chains
-                            float mx[8];
+                    // S row of this thread, all columns at once (216 registers per
+                    // softmax thread leave room for it)
+                    uint32_t sr[128];
+                    if (kt.nkeys == 128) {
+                        tmem_ld128(tS, sr);
+                    } else {
+                        #pragma unroll
+                        for (int g4 = 0; g4 < 8; ++g4)
+                            if (g4 * 16 < kt.nkeys)
+                                tmem_ld16(tS + g4 * 16, *reinterpret_cast<uint32_t(*)[16]>(&sr[g4 * 16]));
+                    }
+                    const bool fast = !masked && kt.nkeys == 128;
+                    if (!fast) {
+                        // invisible or absent columns -> -inf, once
+                        #pragma unroll
+                        for (int c = 0; c < 128; ++c)
+                            if (!((vm[c >> 5] >> (c & 31)) & 1u)) sr[c] = 0xff800000u;
+                    }
+                    // row maximum (raw score units; the scale is positive)
+                    float tmax;
+                    {
+                        float m8[8];
+                        #pragma unroll
+                        for (int a = 0; a < 8; ++a) m8[a] = __uint_as_float(sr[a]);
+                        #pragma unroll
+                        for (int e = 8; e < 128; e += 16)
                             #pragma unroll
-                            for (int a = 0; a < 8; ++a) mx[a] = -INFINITY;
-                            #pragma unroll
-                            for (int e = 0; e < 64; ++e) {
-                                const int c = base + e;
-                                if ((vm[c >> 5] >> (c & 31)) & 1u) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(sr[e]));
-                            }
-                            #pragma unroll
-                            for (int a = 0; a < 4; ++a) mx[a] = fmaxf(mx[a], mx[a + 4]);
-                            mx[0] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-                            tmax = fmaxf(tmax, mx[0] * sl2);
-                        }
+                            for (int a = 0; a < 8; ++a)
+                                m8[a] = fmax3(m8[a], __uint_as_float(sr[e + a]), __uint_as_float(sr[e + 8 + a]));
+                        tmax = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
+                                     fmaxf(m8[6], m8[7])) * sl2;
                     }
                     // online softmax with lazy rescale
                     float alpha = 1.f;
@@ -448,44 +558,41 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                         }
                         tmem_st_wait();
                     }
-                    // pass 2: exponentials, row sum, P row -> shared memory in the
-                    // K-major 128-byte-swizzled operand layout
-                    float rsum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                    // exponentials, row sum, P row -> shared memory in the K-major
+                    // 128-byte-swizzled operand layout (-inf columns give 0).  The
+                    // scale-and-shift and the row sum use packed fp32x2 arithmetic.
+                    uint64_t rsum2[4] = {0ull, 0ull, 0ull, 0ull};
+                    const uint64_t sl2x2 = pack_f32x2(sl2, sl2), nmbx2 = pack_f32x2(-mb, -mb);
                     #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        const int base = half * 64;
-                        if (base < kt.nkeys) {
-                            uint32_t sr[64];
-                            load_s64(tS + base, kt.nkeys - base, sr);
+                    for (int c8 = 0; c8 < 16; ++c8) {
+                        if (c8 * 8 < kt.nkeys) {
+                            uint32_t pk[4];
                             #pragma unroll
-                            for (int c8 = 0; c8 < 8; ++c8) {
-                                if (base + c8 * 8 < kt.nkeys) {
-                                    float pv[8];
-                                    #pragma unroll
-                                    for (int e = 0; e < 8; ++e) {
-                                        const int c = base + c8 * 8 + e;
-                                        pv[e] = ((vm[c >> 5] >> (c & 31)) & 1u)
-                                                    ? fast_exp2(fmaf(__uint_as_float(sr[c8 * 8 + e]), sl2, -mb))
-                                                    : 0.f;
-                                        rsum[e] += pv[e];
-                                    }
-                                    uint4 v;
-                                    v.x = pack_bf16(pv[0], pv[1]);
-                                    v.y = pack_bf16(pv[2], pv[3]);
-                                    v.z = pack_bf16(pv[4], pv[5]);
-                                    v.w = pack_bf16(pv[6], pv[7]);
-                                    *reinterpret_cast<uint4*>(myP + half * S::kHalfBytes +
-                                                              sw128((uint32_t)r, (uint32_t)c8)) = v;
-                                }
+                            for (int e2 = 0; e2 < 4; ++e2) {
+                                const int c = c8 * 8 + 2 * e2;
+                                const uint64_t x2 = fma_f32x2(pack_u32x2(sr[c], sr[c + 1]), sl2x2, nmbx2);
+                                float x0, x1;
+                                unpack_f32x2(x2, x0, x1);
+                                const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                                const uint64_t p2 = pack_f32x2(p0, p1);
+                                rsum2[e2] = add_f32x2(rsum2[e2], p2);
+                                pk[e2] = pack_bf16(p0, p1);
                             }
+                            *reinterpret_cast<uint4*>(myP + (c8 >> 3) * S::kHalfBytes +
+                                                      sw128((uint32_t)r, (uint32_t)(c8 & 7))) =
+                                make_uint4(pk[0], pk[1], pk[2], pk[3]);
                         }
                     }
+                    float rsum[8];
+                    #pragma unroll
+                    for (int e2 = 0; e2 < 4; ++e2) unpack_f32x2(rsum2[e2], rsum[2 * e2], rsum[2 * e2 + 1]);
                     const float rs = ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3])) +
                                      ((rsum[4] + rsum[5]) + (rsum[6] + rsum[7]));
                     l = l * alpha + rs;
                     fence_async_smem();
                     tc_fence_before();
-                    mbar_arrive(&p_full[t]);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&p_full[t]);
                 }
                 if (!ok) break;
                 // epilogue: O / l -> bf16 rows, LSE
@@ -509,7 +616,8 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                     }
                 }
                 tc_fence_before();
-                mbar_arrive(&o_empty[t]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&o_empty[t]);
                 if (row_ok && p.lse)
                     p.lse[(it.row_base + r) * g.hq + head] =
                         l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
