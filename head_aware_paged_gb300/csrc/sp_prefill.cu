@@ -11,16 +11,17 @@
 //                chunk (2D tensor map) or from cache pages (tensor map over
 //                the page pool), 128-byte swizzled, into a ring of stages.
 //   warp 9       TMEM owner and tcgen05 MMA issuer (one thread): S_t = Q_t K^T
-//                into TMEM, later O_t += P_t V with P_t from shared memory.
+//                into TMEM, later O_t += P_t V with P_t read from TMEM.
 //   warps 10-11  idle (the producer/MMA warpgroup gives its registers to the
 //                softmax warpgroups with setmaxnreg).
 //   warps 0-3    softmax + epilogue of query tile 0; warps 4-7 of tile 1.
 //                Each thread owns one query row: it reads its S row from
 //                TMEM into registers, masks (only on tiles that need it, see
 //                sp_plan.h),
-//                keeps the running max / sum, writes P (bf16) into shared
-//                memory in the MMA operand layout, and rescales its O row in
-//                TMEM only when the max grew by more than 2^8 (lazy rescale).
+//                keeps the running max / sum, writes P (bf16 pairs) back into
+//                TMEM over its S tile, where the PV MMA reads it as the A
+//                operand, and rescales its O row in TMEM only when the max
+//                grew by more than 2^8 (lazy rescale).
 //   The two query tiles share every K/V tile and ping-pong on the tensor core:
 //   while one softmax group works, the MMA warp runs the other's PV and next QK.
 // Work items are assigned to CTAs on the host, longest first, each to the
@@ -84,9 +85,8 @@ struct PfShape {
     static constexpr int kHalves = D / 64;
     static constexpr int kHalfBytes = 128 * 128;            // 128 rows x 128 bytes
     static constexpr int kQBytes = kHalves * kHalfBytes;     // one Q tile
-    static constexpr int kPBytes = 2 * kHalfBytes;           // one P tile (128 x 128 bf16)
     static constexpr int kKVBytes = kHalves * kHalfBytes;    // one K or V tile
-    static constexpr int kFixed = 2 * kQBytes + 2 * kPBytes;
+    static constexpr int kFixed = 2 * kQBytes;
     static constexpr int kMisc = 2048;                       // barriers, flags, alignment slack
     static constexpr int kStagesFit = (kSmemLimit - kFixed - kMisc) / kKVBytes;
     static constexpr int kStages = kStagesFit > 6 ? 6 : kStagesFit;
@@ -186,8 +186,7 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = smem;                               // [2][halves][128][128 B]
-    uint8_t* sP = sQ + 2 * S::kQBytes;                // [2][2][128][128 B]
-    uint8_t* sKV = sP + 2 * S::kPBytes;               // [NS][halves][128][128 B]
+    uint8_t* sKV = sQ + 2 * S::kQBytes;               // [NS][halves][128][128 B]
     uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + NS * S::kKVBytes);
     uint64_t* q_full = bars;
     uint64_t* q_empty = bars + 1;
@@ -323,17 +322,15 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
         if (q_loads > 0) mbar_wait(q_full, (q_loads - 1) & 1, nullptr, nullptr);
       } else if (warp == kMmaWarp && lane == 0) {
         // ------------------------------ MMA issuer ------------------------------
-        const uint32_t q_addr = smem_u32(sQ), p_addr = smem_u32(sP), kv_addr = smem_u32(sKV);
+        const uint32_t q_addr = smem_u32(sQ), kv_addr = smem_u32(sKV);
         const uint32_t idesc_pv = idesc_bf16(128, D, true);
         // Descriptors are built once as 32-bit halves; stepping through a tile
         // only adds the byte offset >> 4 to the low half's start-address field
         // (no carry: every tile lies inside the 256 KB shared window).
         const uint64_t dq0 = sdesc_sw128(q_addr, 16, 1024);
-        const uint64_t dp0 = sdesc_sw128(p_addr, 16, 1024);
         const uint64_t dk0 = sdesc_sw128(kv_addr, 16, 1024);
         const uint64_t dv0 = sdesc_sw128(kv_addr, S::kHalfBytes, 1024);
-        const uint32_t q_lo = (uint32_t)dq0, p_lo = (uint32_t)dp0, k_lo = (uint32_t)dk0,
-                       v_lo = (uint32_t)dv0;
+        const uint32_t q_lo = (uint32_t)dq0, k_lo = (uint32_t)dk0, v_lo = (uint32_t)dv0;
         const uint32_t kmaj_hi = (uint32_t)(dq0 >> 32), v_hi = (uint32_t)(dv0 >> 32);
         auto issue_qk = [&](int t, uint32_t st, int nkeys) {
             const uint32_t idesc = idesc_bf16(128, nkeys, false);
@@ -347,21 +344,23 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                 tc_mma_acc(d, a0 + off, kmaj_hi, b0 + off, kmaj_hi, idesc);
             }
         };
+        // O_t (+)= P_t V: P_t sits in TMEM over the first 64 columns of S_t
+        // (16 keys = 8 columns per K step), V from shared memory.  The tensor
+        // core runs this thread's MMAs in issue order, so S_t of the next tile
+        // (issued after this PV) cannot overwrite P_t before it is read.
         auto issue_pv = [&](int t, uint32_t st, int nkeys, bool acc) {
-            const uint32_t a0 = p_lo + ((t * S::kPBytes) >> 4);
+            const uint32_t a0 = tmem + t * 128;
             const uint32_t b0 = v_lo + ((st * S::kKVBytes) >> 4);
             const uint32_t d = tmem + 256 + t * D;
-            if (acc) tc_mma_acc(d, a0, kmaj_hi, b0, v_hi, idesc_pv);
-            else tc_mma_first(d, a0, kmaj_hi, b0, v_hi, idesc_pv);
+            if (acc) tc_mma_ta_acc(d, a0, b0, v_hi, idesc_pv);
+            else tc_mma_ta_first(d, a0, b0, v_hi, idesc_pv);
             if (nkeys == 128) {
                 #pragma unroll
                 for (int ks = 1; ks < 8; ++ks)
-                    tc_mma_acc(d, a0 + (((ks >> 2) * S::kHalfBytes + (ks & 3) * 32) >> 4), kmaj_hi,
-                               b0 + ((ks * 2048) >> 4), v_hi, idesc_pv);
+                    tc_mma_ta_acc(d, a0 + ks * 8, b0 + ((ks * 2048) >> 4), v_hi, idesc_pv);
             } else {
                 for (int ks = 1; ks * 16 < nkeys; ++ks)
-                    tc_mma_acc(d, a0 + (((ks >> 2) * S::kHalfBytes + (ks & 3) * 32) >> 4), kmaj_hi,
-                               b0 + ((ks * 2048) >> 4), v_hi, idesc_pv);
+                    tc_mma_ta_acc(d, a0 + ks * 8, b0 + ((ks * 2048) >> 4), v_hi, idesc_pv);
             }
         };
         uint32_t q_uses = 0, L = 0, e = 0;
@@ -431,7 +430,6 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
             const uint32_t lane_off = ((uint32_t)(warp & 3) * 32u) << 16;
             const uint32_t tS = tmem + lane_off + t * 128;
             const uint32_t tO = tmem + lane_off + 256 + t * D;
-            uint8_t* myP = sP + t * S::kPBytes;
             const float sl2 = p.scale_log2;
             uint32_t k = 0;
             bool ok = true;
@@ -563,38 +561,38 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                     // scale-and-shift and the row sum use packed fp32x2 arithmetic.
                     uint64_t rsum2[4] = {0ull, 0ull, 0ull, 0ull};
                     const uint64_t sl2x2 = pack_f32x2(sl2, sl2), nmbx2 = pack_f32x2(-mb, -mb);
-                    auto exp_chunk = [&](int c8) {
-                        uint32_t pk[4];
+                    // P row as bf16 pairs (column j of the S tile = keys 2j, 2j+1),
+                    // stored to TMEM 32 keys at a time
+                    auto exp_group = [&](int g4) {
+                        uint32_t pk[16];
                         #pragma unroll
-                        for (int e2 = 0; e2 < 4; ++e2) {
-                            const int c = c8 * 8 + 2 * e2;
+                        for (int e2 = 0; e2 < 16; ++e2) {
+                            const int c = g4 * 32 + 2 * e2;
                             const uint64_t x2 = fma_f32x2(pack_u32x2(sr[c], sr[c + 1]), sl2x2, nmbx2);
                             float x0, x1;
                             unpack_f32x2(x2, x0, x1);
                             const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-                            rsum2[e2] = add_f32x2(rsum2[e2], pack_f32x2(p0, p1));
+                            rsum2[e2 & 3] = add_f32x2(rsum2[e2 & 3], pack_f32x2(p0, p1));
                             pk[e2] = pack_bf16(p0, p1);
                         }
-                        *reinterpret_cast<uint4*>(myP + (c8 >> 3) * S::kHalfBytes +
-                                                  sw128((uint32_t)r, (uint32_t)(c8 & 7))) =
-                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        tmem_st16(tS + g4 * 16, pk);
                     };
                     if (kt.nkeys == 128) {
-                        // full tile: no guards, so the compiler can interleave chunks
+                        // full tile: no guards, so the compiler can interleave groups
                         #pragma unroll
-                        for (int c8 = 0; c8 < 16; ++c8) exp_chunk(c8);
+                        for (int g4 = 0; g4 < 4; ++g4) exp_group(g4);
                     } else {
                         #pragma unroll
-                        for (int c8 = 0; c8 < 16; ++c8)
-                            if (c8 * 8 < kt.nkeys) exp_chunk(c8);
+                        for (int g4 = 0; g4 < 4; ++g4)
+                            if (g4 * 32 < kt.nkeys) exp_group(g4);
                     }
+                    tmem_st_wait();
                     float rsum[8];
                     #pragma unroll
                     for (int e2 = 0; e2 < 4; ++e2) unpack_f32x2(rsum2[e2], rsum[2 * e2], rsum[2 * e2 + 1]);
                     const float rs = ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3])) +
                                      ((rsum[4] + rsum[5]) + (rsum[6] + rsum[7]));
                     l = l * alpha + rs;
-                    fence_async_smem();
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&p_full[t]);
