@@ -312,14 +312,16 @@ class DecodeStep:
 # ---------------------------------------------------------------- traffic
 
 def load_traffic(kernel: str, workload: str):
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel sources changed since that capture."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
     try:
         with open(path) as f:
-            d = json.load(f)
-        e = d.get(kernel + "/" + workload)
-        if e and e.get("source_sha") == source_sha():
-            return e.get("bytes_per_launch")
-    except Exception:
+            for line in f:
+                parts = line.split()
+                if len(parts) == 3 and not line.startswith("#") and parts[0] == kernel + "/" + workload:
+                    return int(parts[2]) if parts[1] == source_sha() else None
+    except OSError:
         pass
     return None
 
@@ -346,7 +348,7 @@ def run_ours(args, ws, rank):
     wl = W.WORKLOADS[args.workload]
     decode = wl.decode_steps > 0 and wl.name.startswith("llama3_8b")
     if decode:
-        st = DecodeStep(wl)
+        st = DecodeStep(wl, layers=args.decode_layers or None)
     else:
         layer_pols = W.policies(wl)
         layer = next((l for l, row in enumerate(layer_pols) if any(p.kind == W.GLOBAL for p in row)), 0)
@@ -590,6 +592,8 @@ def main():
     ap.add_argument("--workload", default="mistral7b_prefill_8k",
                     choices=["mistral7b_prefill_8k", "llama3_8b_decode_32k", "llama33_70b_prefill_128k"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-layers", type=int, default=0,
+                    help="decode workload: run only the first N layers (profiling a small case)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
