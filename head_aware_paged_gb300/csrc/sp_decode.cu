@@ -45,7 +45,8 @@ struct DecodeShape {
     static constexpr int kMergeBytes = kConsumerWarps * kMaxGroup * (D + 2) * 4;
     static constexpr int kSmemBytes = kStages * kStageBytes + kMergeBytes
                                       + kStages * 16 /*full, empty*/ + kStages * 16 /*desc*/
-                                      + 64 + 1024 /*alignment slack*/;
+                                      + 16 /*flags*/ + 32 * 16 /*producer batch*/
+                                      + 1024 /*alignment slack*/;
 };
 
 __device__ __forceinline__ int64_t cta_of_item(int64_t x, int64_t T, int G) {
@@ -69,6 +70,7 @@ k_decode(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtenso
     int4* desc = reinterpret_cast<int4*>(empty + NST);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(desc + NST);
     int* flag_last = const_cast<int*>(abort_flag) + 1;
+    int4* batch = reinterpret_cast<int4*>(const_cast<int*>(abort_flag) + 4);   // [32] producer batch
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, c = blockIdx.x;
@@ -86,64 +88,79 @@ k_decode(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtenso
 
     if (warp == kConsumerWarps) {
         // ---------------- producer: stream this CTA's pages ----------------
-        if (lane == 0 && x0 < x1) {
-            prefetch_tmap(&tmK);
-            prefetch_tmap(&tmV);
-            int u = 0;
-            {   // first unit with item_off[u+1] > x0
-                int lo = 0, hi = p.n_units - 1;
-                while (lo < hi) {
-                    const int mid = (lo + hi) >> 1;
-                    if (p.item_off[mid + 1] <= x0) lo = mid + 1; else hi = mid;
-                }
-                u = lo;
-            }
+        // The warp resolves the pages of 32 work items at a time (one per lane:
+        // unit, policy, visible ranges, page-table entry -- dependent global
+        // loads whose latency the lanes overlap), then lane 0 waits for free
+        // stages and issues the TMA loads in item order.
+        if (x0 < x1) {
+            if (lane == 0) { prefetch_tmap(&tmK); prefetch_tmap(&tmV); }
             int64_t issued = 0;
-            for (int64_t x = x0; x < x1; ++x) {
-                while (p.item_off[u + 1] <= x) ++u;
-                const int b = u / g.hkv, h = u % g.hkv;
-                const int seq = p.seq[b];
-                const int64_t row = g.unit_row(seq, p.layer, h);
-                const UnitPol pol = p.meta.pol[row];
-                const int32_t* idx = p.meta.idx + (int64_t)seq * g.max_idx_per_seq + pol.idx_off;
-                const SlotRanges rg = decode_ranges(pol, idx, p.tq[b], P);
-                int64_t j = x - p.item_off[u];
-                int64_t pidx = 0, lo = 0, hi = 0;
-                for (int q = 0; q < rg.count; ++q) {
-                    const int64_t np = range_pages(rg.lo[q], rg.hi[q], P);
-                    if (j < np) {
-                        pidx = rg.lo[q] / P + j;
-                        lo = max64(rg.lo[q], pidx * P) - pidx * P;
-                        hi = min64(rg.hi[q], (pidx + 1) * P) - pidx * P;
-                        break;
+            for (int64_t base = x0; base < x1; base += 32) {
+                const int64_t x = base + lane;
+                if (x < x1) {
+                    int lo_u = 0, hi_u = p.n_units - 1;      // unit holding item x
+                    while (lo_u < hi_u) {
+                        const int mid = (lo_u + hi_u) >> 1;
+                        if (p.item_off[mid + 1] <= x) lo_u = mid + 1; else hi_u = mid;
                     }
-                    j -= np;
+                    const int u = lo_u;
+                    const int b = u / g.hkv, h = u % g.hkv;
+                    const int seq = p.seq[b];
+                    const int64_t row = g.unit_row(seq, p.layer, h);
+                    const UnitPol pol = p.meta.pol[row];
+                    const int32_t* idx = p.meta.idx + (int64_t)seq * g.max_idx_per_seq + pol.idx_off;
+                    const SlotRanges rg = decode_ranges(pol, idx, p.tq[b], P);
+                    int64_t j = x - p.item_off[u];
+                    int64_t pidx = 0, lo = 0, hi = 0;
+                    for (int q = 0; q < rg.count; ++q) {
+                        const int64_t np = range_pages(rg.lo[q], rg.hi[q], P);
+                        if (j < np) {
+                            pidx = rg.lo[q] / P + j;
+                            lo = max64(rg.lo[q], pidx * P) - pidx * P;
+                            hi = min64(rg.hi[q], (pidx + 1) * P) - pidx * P;
+                            break;
+                        }
+                        j -= np;
+                    }
+                    int32_t page = p.meta.ptab[row * g.max_pages_unit + pidx];
+                    if (page < 0 || page >= g.num_pages) {
+                        atomicOr(p.meta.status, kStatusBadPage);
+                        page = 0; lo = hi = 0;          // load something harmless, use nothing
+                    }
+                    batch[lane] = make_int4(u, (int)lo, (int)hi, page);
                 }
-                int32_t page = p.meta.ptab[row * g.max_pages_unit + pidx];
-                if (page < 0 || page >= g.num_pages) {
-                    atomicOr(p.meta.status, kStatusBadPage);
-                    page = 0; lo = hi = 0;              // load something harmless, use nothing
+                __syncwarp();
+                if (lane == 0) {
+                    const int n = (int)min64(32, x1 - base);
+                    for (int i = 0; i < n; ++i) {
+                        const int64_t xi = base + i;
+                        const int64_t k = (xi - x0) / NST;
+                        const int s = (int)((xi - x0) % NST);
+                        if (k > 0 && !mbar_wait(&empty[s], (uint32_t)((k - 1) & 1), abort_flag, p.meta.status))
+                            break;
+                        const int4 bi = batch[i];
+                        desc[s] = make_int4(bi.x, bi.y, bi.z, 0);
+                        mbar_arrive_expect_tx(&full[s], S::kStageBytes);
+                        uint8_t* kdst = stages + s * S::kStageBytes;
+                        uint8_t* vdst = kdst + S::kTileBytes;
+                        #pragma unroll
+                        for (int hh = 0; hh < S::kHalves; ++hh) {
+                            tma_load_2d(kdst + hh * S::kHalfBytes, &tmK, &full[s], hh * 64, bi.w * P);
+                            tma_load_2d(vdst + hh * S::kHalfBytes, &tmV, &full[s], hh * 64, bi.w * P);
+                        }
+                        ++issued;
+                    }
                 }
-                const int64_t k = (x - x0) / NST;
-                const int s = (int)((x - x0) % NST);
-                if (k > 0 && !mbar_wait(&empty[s], (uint32_t)((k - 1) & 1), abort_flag, p.meta.status))
-                    break;
-                desc[s] = make_int4(u, (int)lo, (int)hi, 0);
-                mbar_arrive_expect_tx(&full[s], S::kStageBytes);
-                uint8_t* kdst = stages + s * S::kStageBytes;
-                uint8_t* vdst = kdst + S::kTileBytes;
-                #pragma unroll
-                for (int hh = 0; hh < S::kHalves; ++hh) {
-                    tma_load_2d(kdst + hh * S::kHalfBytes, &tmK, &full[s], hh * 64, page * P);
-                    tma_load_2d(vdst + hh * S::kHalfBytes, &tmV, &full[s], hh * 64, page * P);
-                }
-                ++issued;
+                __syncwarp();
+                if (*abort_flag) break;
             }
             // Leave only after every load this CTA issued has landed (bounded,
             // also after an abort).
-            for (int s = 0; s < NST && s < issued; ++s) {
-                const int64_t last_k = (issued - 1 - s) / NST;
-                mbar_wait(&full[s], (uint32_t)(last_k & 1), nullptr, nullptr);
+            if (lane == 0) {
+                for (int s = 0; s < NST && s < issued; ++s) {
+                    const int64_t last_k = (issued - 1 - s) / NST;
+                    mbar_wait(&full[s], (uint32_t)(last_k & 1), nullptr, nullptr);
+                }
             }
         }
         return;
