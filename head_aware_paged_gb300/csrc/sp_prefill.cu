@@ -163,18 +163,6 @@ __device__ __forceinline__ uint32_t lowmask32(int32_t n) {
     return n <= 0 ? 0u : n >= 32 ? 0xFFFFFFFFu : ((1u << n) - 1u);
 }
 
-// Load columns [0, min(64, n)) of this thread's S row (n > 0, multiple of
-// 16) from TMEM and wait; columns at or past n are left undefined.
-__device__ __forceinline__ void load_s64(uint32_t taddr, int n, uint32_t (&r)[64]) {
-    if (n >= 64) {
-        tmem_ld64(taddr, r);
-    } else {
-        #pragma unroll
-        for (int g4 = 0; g4 < 4; ++g4)
-            if (g4 * 16 < n) tmem_ld16(taddr + g4 * 16, *reinterpret_cast<uint32_t(*)[16]>(&r[g4 * 16]));
-    }
-}
-
 template <int D, int P>
 __global__ void __launch_bounds__(kPfThreads, 1)
 k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tmQ,
@@ -352,8 +340,7 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
             const uint32_t a0 = tmem + t * 128;
             const uint32_t b0 = v_lo + ((st * S::kKVBytes) >> 4);
             const uint32_t d = tmem + 256 + t * D;
-            if (acc) tc_mma_ta_acc(d, a0, b0, v_hi, idesc_pv);
-            else tc_mma_ta_first(d, a0, b0, v_hi, idesc_pv);
+            tc_mma_ta(d, a0, b0, v_hi, idesc_pv, acc ? 1u : 0u);
             if (nkeys == 128) {
                 #pragma unroll
                 for (int ks = 1; ks < 8; ++ks)
@@ -363,8 +350,7 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                     tc_mma_ta_acc(d, a0 + ks * 8, b0 + ((ks * 2048) >> 4), v_hi, idesc_pv);
             }
         };
-        uint32_t q_uses = 0, L = 0, e = 0;
-        uint32_t tiles_t[2] = {0, 0};
+        uint32_t q_uses = 0, L = 0, e = 0, tiles = 0;   // both query tiles see every K/V tile
         bool ok = true;
         for (int n = p.cta_off[cta]; n < p.cta_off[cta + 1] && ok; ++n) {
             const Item it = load_item(p, n);
@@ -398,16 +384,16 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                     ++L;
                 }
                 for (int t = 0; t < nq && ok; ++t) {
-                    if (!mbar_wait(&p_full[t], tiles_t[t] & 1, abort_flag, status)) { ok = false; break; }
+                    if (!mbar_wait(&p_full[t], tiles & 1, abort_flag, status)) { ok = false; break; }
                     if (j == 0 && e > 0 &&
                         !mbar_wait(&o_empty[t], (e - 1) & 1, abort_flag, status)) { ok = false; break; }
                     tc_fence_after();
                     issue_pv(t, stV, kt.nkeys, j > 0);
                     tc_commit(&o_full[t]);
-                    ++tiles_t[t];
                     if (j + 1 < nt) { issue_qk(t, stK2, kn.nkeys); tc_commit(&s_full[t]); }
                 }
                 if (!ok) break;
+                ++tiles;
                 tc_commit(&kv_empty[stV]);
                 if (j + 1 < nt) {
                     tc_commit(&kv_empty[stK2]);
@@ -494,17 +480,14 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                             vm[w] = b;
                         }
                     }
-                    // S row of this thread, all columns at once (216 registers per
-                    // softmax thread leave room for it)
+                    // S row of this thread, all 128 columns at once (the softmax
+                    // warpgroups hold 208 registers a thread).  Columns at or past
+                    // nkeys were not written by this tile's MMA and hold stale
+                    // values; their visibility bits are 0, so the select below
+                    // turns them into -inf like any invisible key.  One code path
+                    // for every tile width keeps the loop small.
                     uint32_t sr[128];
-                    if (kt.nkeys == 128) {
-                        tmem_ld128(tS, sr);
-                    } else {
-                        #pragma unroll
-                        for (int g4 = 0; g4 < 8; ++g4)
-                            if (g4 * 16 < kt.nkeys)
-                                tmem_ld16(tS + g4 * 16, *reinterpret_cast<uint32_t(*)[16]>(&sr[g4 * 16]));
-                    }
+                    tmem_ld128(tS, sr);
                     const bool fast = !masked && kt.nkeys == 128;
                     if (!fast) {
                         // invisible or absent columns -> -inf, once (branch-free)
@@ -577,25 +560,22 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                         }
                         tmem_st16(tS + g4 * 16, pk);
                     };
-                    if (kt.nkeys == 128) {
-                        // full tile: no guards, so the compiler can interleave groups
-                        #pragma unroll
-                        for (int g4 = 0; g4 < 4; ++g4) exp_group(g4);
-                    } else {
-                        #pragma unroll
-                        for (int g4 = 0; g4 < 4; ++g4)
-                            if (g4 * 32 < kt.nkeys) exp_group(g4);
-                    }
+                    // all four groups on every tile (no guards, so the compiler can
+                    // interleave them): past nkeys the row is -inf, P is 0 there,
+                    // and the PV MMA reads only the first nkeys / 2 columns
+                    #pragma unroll
+                    for (int g4 = 0; g4 < 4; ++g4) exp_group(g4);
                     tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&p_full[t]);
+                    // the row sum is not needed by the MMA: fold it after the arrive
                     float rsum[8];
                     #pragma unroll
                     for (int e2 = 0; e2 < 4; ++e2) unpack_f32x2(rsum2[e2], rsum[2 * e2], rsum[2 * e2 + 1]);
                     const float rs = ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3])) +
                                      ((rsum[4] + rsum[5]) + (rsum[6] + rsum[7]));
                     l = l * alpha + rs;
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&p_full[t]);
                 }
                 if (!ok) break;
                 // epilogue: O / l -> bf16 rows, LSE

@@ -93,6 +93,17 @@ __device__ __forceinline__ void tc_mma_ta_first(uint32_t d_tmem, uint32_t a_tmem
                  ::"r"(d_tmem), "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc) : "memory");
 }
 
+// ... accumulating into D when `accumulate` is non-zero, overwriting it
+// otherwise (a predicate, so no branch separates it from its neighbours).
+__device__ __forceinline__ void tc_mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                          uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+    asm volatile("{\n\t.reg .b64 db;\n\t.reg .pred p;\n\tsetp.ne.b32 p, %5, 0;\n\t"
+                 "mov.b64 db, {%2, %3};\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}"
+                 ::"r"(d_tmem), "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
 // Shared-memory descriptor of a 128-byte-swizzled operand tile.
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes,
                                                uint32_t sbo_bytes) {
