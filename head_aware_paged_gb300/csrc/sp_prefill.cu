@@ -350,6 +350,15 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                     tc_mma_ta_acc(d, a0 + ks * 8, b0 + ((ks * 2048) >> 4), v_hi, idesc_pv);
             }
         };
+        auto issue_pv_full = [&](int t, uint32_t st, bool acc) {
+            const uint32_t a0 = tmem + t * 128;
+            const uint32_t b0 = v_lo + ((st * S::kKVBytes) >> 4);
+            const uint32_t d = tmem + 256 + t * D;
+            tc_mma_ta(d, a0, b0, v_hi, idesc_pv, acc ? 1u : 0u);
+            #pragma unroll
+            for (int ks = 1; ks < 8; ++ks)
+                tc_mma_ta_acc(d, a0 + ks * 8, b0 + ((ks * 2048) >> 4), v_hi, idesc_pv);
+        };
         uint32_t q_uses = 0, L = 0, e = 0, tiles = 0;   // both query tiles see every K/V tile
         bool ok = true;
         for (int n = p.cta_off[cta]; n < p.cta_off[cta + 1] && ok; ++n) {
@@ -383,16 +392,29 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                     if (!mbar_wait(&kv_full[stK2], (L / NS) & 1, abort_flag, status)) { ok = false; break; }
                     ++L;
                 }
-                for (int t = 0; t < nq && ok; ++t) {
-                    if (!mbar_wait(&p_full[t], tiles & 1, abort_flag, status)) { ok = false; break; }
-                    if (j == 0 && e > 0 &&
-                        !mbar_wait(&o_empty[t], (e - 1) & 1, abort_flag, status)) { ok = false; break; }
+                const bool first = j == 0 && e > 0;     // O_t still holds the last item
+                const bool steady = kt.nkeys == 128 && j + 1 < nt;
+                // Per query tile: PV of this tile, then QK of the next.  In the
+                // steady state the 16 MMAs and their commits are one straight
+                // run of code: a branch between two MMAs costs the tensor core
+                // tens of cycles of issue.
+                auto step = [&](int t) -> bool {
+                    if (!mbar_wait(&p_full[t], tiles & 1, abort_flag, status)) return false;
+                    if (first && !mbar_wait(&o_empty[t], (e - 1) & 1, abort_flag, status)) return false;
                     tc_fence_after();
-                    issue_pv(t, stV, kt.nkeys, j > 0);
-                    tc_commit(&o_full[t]);
-                    if (j + 1 < nt) { issue_qk(t, stK2, kn.nkeys); tc_commit(&s_full[t]); }
-                }
-                if (!ok) break;
+                    if (steady) {
+                        issue_pv_full(t, stV, j > 0);
+                        tc_commit(&o_full[t]);
+                        issue_qk(t, stK2, kn.nkeys);
+                        tc_commit(&s_full[t]);
+                    } else {
+                        issue_pv(t, stV, kt.nkeys, j > 0);
+                        tc_commit(&o_full[t]);
+                        if (j + 1 < nt) { issue_qk(t, stK2, kn.nkeys); tc_commit(&s_full[t]); }
+                    }
+                    return true;
+                };
+                if (!step(0) || (nq > 1 && !step(1))) { ok = false; break; }
                 ++tiles;
                 tc_commit(&kv_empty[stV]);
                 if (j + 1 < nt) {
