@@ -284,6 +284,14 @@ sp_status sp_cache_create(const sp_config* cfg, void* pool, void* meta, void* ws
     // Device state: every page free, all units empty, the pool zeroed (slots
     // past a page's valid range are read by the kernels and multiplied by a
     // zero weight, so they must hold finite values).
+    // pinned host staging ring for the prefill work list (host memory: the
+    // device buffers stay the caller's)
+    for (int i = 0; i < sp_cache::kStaging && e == cudaSuccess; ++i) {
+        e = cudaHostAlloc(reinterpret_cast<void**>(&c->stage_buf[i]), (size_t)L.max_tiles * sizeof(int4),
+                          cudaHostAllocDefault);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->stage_ev[i], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) { delete c; return cuda_fail(e, "pinned staging buffers"); }
     e = cudaMemset(meta, 0, L.meta_total);
     if (e == cudaSuccess) e = cudaMemset(ws, 0, L.ws_total);
     if (e == cudaSuccess) e = cudaMemset(pool, 0, L.pool_total);
@@ -299,6 +307,16 @@ sp_status sp_cache_create(const sp_config* cfg, void* pool, void* meta, void* ws
     c->h_free = cfg->num_pages;
     *out = c;
     return SP_OK;
+}
+
+sp_cache::~sp_cache() {
+    for (int i = 0; i < kStaging; ++i) {
+        if (stage_ev[i]) {
+            cudaEventSynchronize(stage_ev[i]);   // no copy may still read the buffer
+            cudaEventDestroy(stage_ev[i]);
+        }
+        if (stage_buf[i]) cudaFreeHost(stage_buf[i]);
+    }
 }
 
 sp_status sp_cache_destroy(sp_cache* cache) {
@@ -417,8 +435,10 @@ sp_status sp_attention_prefill(sp_cache* c, int32_t layer, const int32_t* seq_id
     sp_status s = check_seq_list(c, seq_ids, n_seqs);
     if (s != SP_OK) return s;
     if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
-         reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out)) & 15)
-        return fail(SP_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned");
+         reinterpret_cast<uintptr_t>(v)) & 15)
+        return fail(SP_ERR_INVALID_ARG, "q, k and v must be 16-byte aligned");
+    if (reinterpret_cast<uintptr_t>(out) & 31)   // the epilogue writes 32-byte vectors
+        return fail(SP_ERR_INVALID_ARG, "out must be 32-byte aligned");
     if (cu_q[0] != 0) return fail(SP_ERR_INVALID_ARG, "cu_q[0] must be 0");
     for (int b = 0; b < n_seqs; ++b) {
         if (cu_q[b + 1] < cu_q[b]) return fail(SP_ERR_INVALID_ARG, "cu_q must be non-decreasing");

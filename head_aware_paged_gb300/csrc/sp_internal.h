@@ -98,6 +98,15 @@ struct sp_cache {
     std::vector<int32_t> h_seqlen;               // [max_seqs][layers]
     std::vector<int32_t> h_npages;               // [max_seqs][layers][hkv]
     int64_t h_free = 0;
+    // Pinned host staging for the per-call prefill work list, so its upload is
+    // an asynchronous copy and the host never waits for the device.  A ring:
+    // a buffer is refilled only after the copy that last read it has run.
+    static constexpr int kStaging = 4;
+    int4* stage_buf[kStaging] = {};
+    cudaEvent_t stage_ev[kStaging] = {};
+    int stage_next = 0;
+    bool prefill_checked[2][4] = {};             // [D == 128][log2(P) - 4]: attributes set
+    ~sp_cache();
 };
 
 namespace sp {

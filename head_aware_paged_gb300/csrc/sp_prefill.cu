@@ -604,25 +604,26 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                 if (!mbar_wait(&o_full[t], (k - 1) & 1, abort_flag, status)) { ok = false; break; }
                 tc_fence_after();
                 const float inv = l > 0.f ? 1.f / l : 0.f;
-                #pragma unroll
-                for (int half = 0; half < D / 64; ++half) {
-                    uint32_t orr[64];
-                    tmem_ld64(tO + half * 64, orr);
-                    if (row_ok) {
-                        #pragma unroll
-                        for (int c = 0; c < 64; c += 8) {
-                            uint4 v;
-                            v.x = pack_bf16(__uint_as_float(orr[c + 0]) * inv, __uint_as_float(orr[c + 1]) * inv);
-                            v.y = pack_bf16(__uint_as_float(orr[c + 2]) * inv, __uint_as_float(orr[c + 3]) * inv);
-                            v.z = pack_bf16(__uint_as_float(orr[c + 4]) * inv, __uint_as_float(orr[c + 5]) * inv);
-                            v.w = pack_bf16(__uint_as_float(orr[c + 6]) * inv, __uint_as_float(orr[c + 7]) * inv);
-                            *reinterpret_cast<uint4*>(orow + half * 64 + c) = v;
-                        }
-                    }
-                }
+                // The whole O row into registers first, then O_t is released at
+                // once (the next item's first PV may overwrite it) and the row
+                // is normalised and written with 32-byte stores.
+                uint32_t orr[D];
+                if constexpr (D == 128) tmem_ld128(tO, *reinterpret_cast<uint32_t(*)[128]>(orr));
+                else tmem_ld64(tO, *reinterpret_cast<uint32_t(*)[64]>(orr));
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&o_empty[t]);
+                if (row_ok) {
+                    #pragma unroll
+                    for (int c = 0; c < D; c += 16) {
+                        uint32_t w[8];
+                        #pragma unroll
+                        for (int e2 = 0; e2 < 8; ++e2)
+                            w[e2] = pack_bf16(__uint_as_float(orr[c + 2 * e2]) * inv,
+                                              __uint_as_float(orr[c + 2 * e2 + 1]) * inv);
+                        st_global_v8(orow + c, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+                    }
+                }
                 if (row_ok && p.lse)
                     p.lse[(it.row_base + r) * g.hq + head] =
                         l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
@@ -664,18 +665,22 @@ __global__ void k_prefill_counts(Meta meta, Geo g, int seq, int layer, int h,
 }
 
 template <int D, int P>
-cudaError_t launch_prefill_t(const sp_cache* c, const PrefillParams& p, int grid,
+cudaError_t launch_prefill_t(sp_cache* c, const PrefillParams& p, int grid,
                              const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                              cudaStream_t s) {
     using Sh = PfShape<D>;
-    cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, k_prefill<D, P>);
-    if (e != cudaSuccess) return e;
-    // The setmaxnreg split assumes exactly kLaunchRegs registers per thread at
-    // launch; anything else could leave an increase waiting forever.
-    if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(k_prefill<D, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmem);
-    if (e != cudaSuccess) return e;
+    bool& checked = c->prefill_checked[D == 128][P == 16 ? 0 : P == 32 ? 1 : P == 64 ? 2 : 3];
+    if (!checked) {   // once per cache and kernel instance
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, k_prefill<D, P>);
+        if (e != cudaSuccess) return e;
+        // The setmaxnreg split assumes exactly kLaunchRegs registers per thread
+        // at launch; anything else could leave an increase waiting forever.
+        if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(k_prefill<D, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmem);
+        if (e != cudaSuccess) return e;
+        checked = true;
+    }
     k_prefill<D, P><<<grid, kPfThreads, Sh::kSmem, s>>>(p, tq, tk, tv, c->tm_kpool, c->tm_vpool);
     return cudaGetLastError();
 }
@@ -749,10 +754,17 @@ sp_status prefill_impl(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32
             heap.push(top);
         }
     }
-    // one upload: the items grouped by CTA, then the CTA offsets
+    // one upload: the items grouped by CTA, then the CTA offsets, through the
+    // next pinned staging buffer (asynchronous; waits only if that buffer's
+    // previous copy has not run yet)
     const size_t n_items = cands.size();
-    std::vector<int4> buf(n_items + (grid + 1 + 3) / 4);
-    int32_t* off = reinterpret_cast<int32_t*>(buf.data() + n_items);
+    const size_t words = n_items + (grid + 1 + 3) / 4;
+    const int si = c->stage_next;
+    c->stage_next = (si + 1) % sp_cache::kStaging;
+    cudaError_t e = cudaEventSynchronize(c->stage_ev[si]);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill staging buffer");
+    int4* buf = c->stage_buf[si];
+    int32_t* off = reinterpret_cast<int32_t*>(buf + n_items);
     size_t pos = 0;
     for (int g2 = 0; g2 < grid; ++g2) {
         off[g2] = (int32_t)pos;
@@ -762,8 +774,8 @@ sp_status prefill_impl(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32
     p.items = c->ws.tiles;
     p.cta_off = reinterpret_cast<const int32_t*>(c->ws.tiles + n_items);
     p.n_items = (int32_t)n_items;
-    cudaError_t e = cudaMemcpyAsync(c->ws.tiles, buf.data(), buf.size() * sizeof(int4),
-                                    cudaMemcpyHostToDevice, stream);
+    e = cudaMemcpyAsync(c->ws.tiles, buf, words * sizeof(int4), cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess) e = cudaEventRecord(c->stage_ev[si], stream);
     if (e != cudaSuccess) return cuda_fail(e, "prefill work list upload");
     CUtensorMap tq, tk, tv;
     std::string err;

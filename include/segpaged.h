@@ -101,7 +101,11 @@ sp_status sp_required_bytes(const sp_config* cfg, size_t* pool_bytes,
 
 /* Create a handle over caller-owned buffers (each 1024-byte aligned, at least
  * the sizes above, on the current CUDA device).  Initialises meta (all units
- * empty, every page free) and waits for that to finish: synchronous. */
+ * empty, every page free) and waits for that to finish: synchronous.  The
+ * handle owns a few small pinned HOST buffers (4 x the prefill work list, at
+ * most a few MB) so that sp_attention_prefill uploads its work list without
+ * blocking the host; sp_cache_destroy waits for their last copies and frees
+ * them.  No device memory is allocated. */
 sp_status sp_cache_create(const sp_config* cfg, void* pool, void* meta, void* ws,
                           sp_cache** out);
 
@@ -140,8 +144,10 @@ sp_status sp_append_kv(sp_cache* cache, int32_t layer, const int32_t* seq_ids,
  * already holds; keys below n_b come from the cache pages, the rest from the
  * chunk's own k, v (same row layout as q's rows, num_kv_heads heads).  Each
  * query head attends over exactly its KV head's visible set; no mask tensor.
- * out [cu_q[n_seqs]][num_q_heads][head_dim] bf16; lse nullable.  Does not
- * modify the cache: call sp_append_kv with the same k, v afterwards. */
+ * out [cu_q[n_seqs]][num_q_heads][head_dim] bf16; lse nullable.  q, k and v
+ * must be 16-byte aligned and out 32-byte aligned (SP_ERR_INVALID_ARG
+ * otherwise).  Does not modify the cache: call sp_append_kv with the same
+ * k, v afterwards. */
 sp_status sp_attention_prefill(sp_cache* cache, int32_t layer,
                                const int32_t* seq_ids, int32_t n_seqs,
                                const int32_t* cu_q, const void* q,

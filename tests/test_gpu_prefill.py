@@ -173,6 +173,29 @@ def test_edge_cases():
     assert cache.status() == 0
 
 
+def test_prefill_rejects_out_not_32_byte_aligned():
+    """out is written with 32-byte vector stores: a 16-byte offset is refused
+    before anything is launched, and the aligned call still works."""
+    gpu_ready()
+    from head_aware_paged_gb300 import SegPagedError
+    d, P = 64, 16
+    cache = _mk(1, 2, 1, d, P, 1, 128, 64)
+    cache.set_policy(0, to_c_policies([[W.HeadPolicy(G)]]))
+    n = 32
+    q = W.normal((n, 2, d), 4, device="cuda")
+    k = W.normal((n, 1, d), 5, device="cuda")
+    v = W.normal((n, 1, d), 6, device="cuda")
+    buf = torch.empty(n * 2 * d + 16, dtype=torch.bfloat16, device="cuda")
+    assert buf.data_ptr() % 32 == 0
+    bad = buf[8:8 + n * 2 * d].view(n, 2, d)          # 16 bytes past a 32-byte boundary
+    with pytest.raises(SegPagedError, match="32-byte"):
+        cache.prefill(0, [0], [0, n], q, k, v, bad)
+    o, lse = cache.prefill(0, [0], [0, n], q, k, v)
+    ref, lref = oracle.attend(f64(q), f64(k), f64(v), np.arange(n), [pol_tuple(W.HeadPolicy(G))], "f64")
+    compare(o, ref, lse, lref, "aligned out after a refused call")
+    assert cache.status() == 0
+
+
 def test_llama33_70b_shape_sampled():
     """Llama-3.3-70B-shaped layer at full size: Hq 64 / Hkv 8, d 128, L 131072,
     LOCAL(4, 8192) and GLOBAL heads, one-shot causal prefill of one layer in the
