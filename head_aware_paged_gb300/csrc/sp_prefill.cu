@@ -70,7 +70,7 @@ struct PrefillParams {
     int32_t nq;                  // query tiles per item: 2 (head pairs) or 1
     int32_t n_items;
     float scale_log2;            // log2(e) / sqrt(d)
-    const int4* items;           // {b, kv head, head pair, row block}, grouped by CTA
+    const int4* items;           // {b, kv head, pair | row block << 8, tiles}, grouped by CTA
     const int32_t* cta_off;      // items of CTA c: [cta_off[c], cta_off[c+1])
     __nv_bfloat16* out;
     float* lse;
@@ -109,9 +109,9 @@ __device__ __forceinline__ Item load_item(const PrefillParams& p, int n) {
     m.b = it.x;
     m.kvh = it.y;
     const Geo& g = p.geo;
-    m.h0 = it.y * g.group + it.z * p.nq;
+    m.h0 = it.y * g.group + (it.z & 255) * p.nq;
     const int seq = p.seq[m.b];
-    const int r0 = it.w * 128;
+    const int r0 = (it.z >> 8) * 128;
     m.rows = min(128, p.cnt[m.b] - r0);
     m.n_b = p.n_b[m.b];
     m.i_lo = m.n_b + r0;
@@ -187,6 +187,10 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
     uint64_t* mma_done = o_empty + 2;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mma_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    // MMA width (keys) of the tile each K/V stage holds, written by the
+    // producer before the stage's copies; read by the MMA thread after the
+    // stage's full barrier (the arrive orders the write before it)
+    volatile int32_t* stage_keys = abort_flag + 4;
     int* status = p.meta.status;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -282,6 +286,7 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                 for (int kv = 0; kv < 2; ++kv) {
                     const uint32_t st = L % NS, rd = L / NS;
                     if (rd > 0 && !mbar_wait(&kv_empty[st], (rd - 1) & 1, abort_flag, status)) { ok = false; break; }
+                    stage_keys[st] = kt.nkeys;
                     uint8_t* dst = sKV + st * S::kKVBytes;
                     if (!kt.paged) {
                         mbar_arrive_expect_tx(&kv_full[st], S::kKVBytes);
@@ -359,41 +364,41 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
             for (int ks = 1; ks < 8; ++ks)
                 tc_mma_ta_acc(d, a0 + ks * 8, b0 + ((ks * 2048) >> 4), v_hi, idesc_pv);
         };
+        // The MMA thread keeps no plan: the host put each item's tile count in
+        // its work entry and the producer writes each stage's key width next to
+        // the stage, so between two tiles this thread only waits and issues.
         uint32_t q_uses = 0, L = 0, e = 0, tiles = 0;   // both query tiles see every K/V tile
         bool ok = true;
-        for (int n = p.cta_off[cta]; n < p.cta_off[cta + 1] && ok; ++n) {
-            const Item it = load_item(p, n);
-            const Plan pl = make_plan(it.pol, it.idx, it.n_b, it.i_lo, it.i_hi, P);
-            const int64_t nt = pl.ntiles;
+        const int n_end = p.cta_off[cta + 1];
+        for (int n = p.cta_off[cta]; n < n_end && ok; ++n) {
+            const int nt = __ldg(&p.items[n].w);
             if (nt == 0) continue;
             if (!mbar_wait(q_full, q_uses & 1, abort_flag, status)) { ok = false; break; }
             ++q_uses;
-            const int32_t ilo32 = (int32_t)it.i_lo, ihi32 = (int32_t)it.i_hi;
-            TileCursor cur = cursor_begin(pl);
-            KvTile kt = cursor_tile(cur, it.pol, ilo32, ihi32);
-            cursor_next(pl, cur);
-            uint32_t stK = L % NS;
+            const uint32_t stK = L % NS;
             if (!mbar_wait(&kv_full[stK], (L / NS) & 1, abort_flag, status)) { ok = false; break; }
             ++L;
+            const int nk0 = stage_keys[stK];
             tc_fence_after();
-            for (int t = 0; t < nq; ++t) { issue_qk(t, stK, kt.nkeys); tc_commit(&s_full[t]); }
+            for (int t = 0; t < nq; ++t) { issue_qk(t, stK, nk0); tc_commit(&s_full[t]); }
             tc_commit(&kv_empty[stK]);
             if (nt == 1) tc_commit(q_empty);
-            for (int64_t j = 0; j < nt && ok; ++j) {
+            for (int j = 0; j < nt && ok; ++j) {
                 const uint32_t stV = L % NS;
                 if (!mbar_wait(&kv_full[stV], (L / NS) & 1, abort_flag, status)) { ok = false; break; }
                 ++L;
-                KvTile kn = kt;
+                const int nkv = stage_keys[stV];          // width of tile j
+                const bool more = j + 1 < nt;
                 uint32_t stK2 = 0;
-                if (j + 1 < nt) {
-                    kn = cursor_tile(cur, it.pol, ilo32, ihi32);
-                    cursor_next(pl, cur);
+                int nk2 = 0;
+                if (more) {
                     stK2 = L % NS;
                     if (!mbar_wait(&kv_full[stK2], (L / NS) & 1, abort_flag, status)) { ok = false; break; }
                     ++L;
+                    nk2 = stage_keys[stK2];                // width of tile j + 1
                 }
                 const bool first = j == 0 && e > 0;     // O_t still holds the last item
-                const bool steady = kt.nkeys == 128 && j + 1 < nt;
+                const bool steady = nkv == 128 && more;
                 // Per query tile: PV of this tile, then QK of the next.  In the
                 // steady state the 16 MMAs and their commits are one straight
                 // run of code: a branch between two MMAs costs the tensor core
@@ -405,23 +410,22 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                     if (steady) {
                         issue_pv_full(t, stV, j > 0);
                         tc_commit(&o_full[t]);
-                        issue_qk(t, stK2, kn.nkeys);
+                        issue_qk(t, stK2, nk2);
                         tc_commit(&s_full[t]);
                     } else {
-                        issue_pv(t, stV, kt.nkeys, j > 0);
+                        issue_pv(t, stV, nkv, j > 0);
                         tc_commit(&o_full[t]);
-                        if (j + 1 < nt) { issue_qk(t, stK2, kn.nkeys); tc_commit(&s_full[t]); }
+                        if (more) { issue_qk(t, stK2, nk2); tc_commit(&s_full[t]); }
                     }
                     return true;
                 };
                 if (!step(0) || (nq > 1 && !step(1))) { ok = false; break; }
                 ++tiles;
                 tc_commit(&kv_empty[stV]);
-                if (j + 1 < nt) {
+                if (more) {
                     tc_commit(&kv_empty[stK2]);
                     if (j + 2 == nt) tc_commit(q_empty);
                 }
-                kt = kn;
             }
             ++e;
         }
@@ -729,7 +733,8 @@ sp_status prefill_impl(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32
                 const int64_t i_hi = n_b + std::min(cb, rb * 128 + 128) - 1;
                 const Plan pl = make_plan(u, idx, n_b, i_lo, i_hi, P);
                 const int64_t cost = plan_cost(pl) + 64;
-                for (int pr = 0; pr < pairs; ++pr) cands.push_back({cost, make_int4(b, h, pr, rb)});
+                for (int pr = 0; pr < pairs; ++pr)
+                    cands.push_back({cost, make_int4(b, h, pr | (rb << 8), (int)pl.ntiles)});
             }
         }
     }
