@@ -326,6 +326,14 @@ def load_traffic(kernel: str, workload: str):
     return None
 
 
+def bench_layer(wl) -> int:
+    """The prefill step runs one layer: the first whose policy has a GLOBAL KV
+    head (every layer has the same shapes; this one carries the full-causal
+    work), else layer 0."""
+    pols = W.policies(wl)
+    return next((l for l, row in enumerate(pols) if any(p.kind == W.GLOBAL for p in row)), 0)
+
+
 def source_sha():
     import hashlib
     h = hashlib.sha1()
@@ -350,9 +358,8 @@ def run_ours(args, ws, rank):
     if decode:
         st = DecodeStep(wl, layers=args.decode_layers or None)
     else:
-        layer_pols = W.policies(wl)
-        layer = next((l for l, row in enumerate(layer_pols) if any(p.kind == W.GLOBAL for p in row)), 0)
-        st = PrefillStep(wl, layer_pols[layer])
+        layer = bench_layer(wl)
+        st = PrefillStep(wl, W.policies(wl)[layer])
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
     for _ in range(args.warmup):
@@ -493,8 +500,9 @@ def config_dict(wl, decode, st):
                   "global_units": wl.n_global, "local": [wl.local_sink, wl.local_window],
                   "step": "all layers: append 1 token/seq + split-KV decode"})
     else:
-        d.update({"seq_len": wl.seq_len, "global_kv_heads_in_layer": sum(
-            1 for p in W.policies(wl)[0] if p.kind == W.GLOBAL),
+        layer = bench_layer(wl)
+        d.update({"seq_len": wl.seq_len, "layer": layer, "global_kv_heads_in_layer": sum(
+            1 for p in W.policies(wl)[layer] if p.kind == W.GLOBAL),
                   "local": [wl.local_sink, wl.local_window],
                   "step": "prefill + trimmed KV write + 1 decode token + release"})
     return d
@@ -552,9 +560,7 @@ def run_reference(args, ws, rank):
         unit, scale, sample = "GB/s", 1e-9, "one decode query of one sequence, layer 0, fp32 C oracle"
     else:
         L = wl.seq_len
-        pol = W.policies(wl)
-        layer = next((l for l, row in enumerate(pol) if any(p.kind == W.GLOBAL for p in row)), 0)
-        pt = [(p.kind, p.sink, p.window, None) for p in pol[layer]]
+        pt = [(p.kind, p.sink, p.window, None) for p in W.policies(wl)[bench_layer(wl)]]
         q, k, v = (t.float().numpy() for t in W.qkv(wl, L, 0, 0))
         grp = wl.hq // wl.hkv
         nrows = 48
