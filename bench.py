@@ -589,6 +589,67 @@ def run_reference(args, ws, rank):
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def stored_rows(pols_row, n: int, seqs: int, page: int) -> int:
+    """K rows one layer stores for `seqs` sequences of n tokens (page rules:
+    GLOBAL n, LOCAL sink + its ring of ceil(W / P) + 1 pages, RETRIEVAL the
+    listed positions below n)."""
+    rows = 0
+    for p in pols_row:
+        if p.kind == W.GLOBAL:
+            rows += n
+        elif p.kind == W.LOCAL:
+            ring = (-(-p.window // page) + 1) * page
+            rows += min(n, p.sink) + min(max(n - p.sink, 0), ring)
+        else:
+            rows += int((np.asarray(p.idx) < n).sum())
+    return rows * seqs
+
+
+def run_op_rope(args):
+    """sp_rope_realign over every stored K row of one layer of the
+    Llama-3-8B-shaped decode batch (32 sequences x 32,768 tokens): HBM-bound,
+    2 * 2d bytes per rotated row (read + write)."""
+    import torch
+    wl = W.WORKLOADS["llama3_8b_decode_32k"]
+    st = DecodeStep(wl, layers=1)
+    c = st.cache
+    nbytes = stored_rows(st.pols[0], st.n, st.B, wl.page) * 2 * wl.d * 2
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup):
+        c.rope_realign(0, st.seqs, 1000)
+    torch.cuda.synchronize()
+    peaks, src = load_peaks()
+    props = torch.cuda.get_device_properties(0)
+    u = str(getattr(props, "uuid", ""))
+    clocks = ClockSampler(u if u.startswith("GPU-") else ("GPU-" + u if u else None))
+    clocks.start()
+    time.sleep(0.4)
+    ms = []
+    for _ in range(args.steps):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        c.rope_realign(0, st.seqs, 1000)
+        b.record()
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    clk = clocks.stop()
+    assert c.status() == 0
+    total = sum(ms)
+    gbs = nbytes * args.steps / (total / 1e3) / 1e9
+    peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    return {"metric": "RoPE realignment of stored K rows, GB/s moved (read + write)",
+            "op": "rope_realign", "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total / args.steps, "higher_is_better": True,
+            "dtype": "bf16", "data": "synthetic (seeded N(0,1), pages' shapes)",
+            "config": {"workload": "llama3_8b_decode_32k, layer 0, all 32 sequences",
+                       "bytes_per_call": nbytes, "l2": "flushed between calls"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                         "frac": gbs / peak, "traffic": None, "kernel": "k_rope",
+                         "peak_source": "%s hbm_gbs" % src},
+            "clocks": clk}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -600,9 +661,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-layers", type=int, default=0,
                     help="decode workload: run only the first N layers (profiling a small case)")
+    ap.add_argument("--op", default="", choices=["", "rope_realign"],
+                    help="time one library operation instead of the attention step")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.op:
+        line = {"rope_realign": run_op_rope}[args.op](args)
+        print(json.dumps(line), flush=True)
+        return
     if args.impl == "reference":
         ws = int(os.environ.get("WORLD_SIZE", "1"))
         rank = int(os.environ.get("RANK", "0"))

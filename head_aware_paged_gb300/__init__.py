@@ -143,6 +143,12 @@ def sp_attention_decode_static_scratch(handle, layer: int, seq_ids: Sequence[int
                                                     _stream(stream)))
 
 
+def sp_rope_realign(handle, layer: int, seq_ids: Sequence[int], kv_head: int, pos_lo: int,
+                    pos_hi: int, delta: int, rope_theta: float = 10000.0, stream=None) -> None:
+    check(load().sp_rope_realign(handle, layer, i32_array(seq_ids), len(seq_ids), kv_head,
+                                 pos_lo, pos_hi, delta, float(rope_theta), _stream(stream)))
+
+
 def sp_release_seq(handle, seq: int, stream=None) -> None:
     check(load().sp_release_seq(handle, seq, _stream(stream)))
 
@@ -278,6 +284,13 @@ class SegPagedCache:
             lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
         sp_attention_decode(self.handle, layer, seq_ids, q, out, lse, stream)
         return out, lse
+
+    def rope_realign(self, layer: int, seq_ids, delta: int, kv_head: int = -1, pos_lo: int = 0,
+                     pos_hi: int = 1 << 62, rope_theta: float = 10000.0, stream=None) -> None:
+        """Rotate the stored K rows at positions [pos_lo, pos_hi) by `delta`
+        positions of rotary embedding (see sp_rope_realign in the C header)."""
+        sp_rope_realign(self.handle, layer, seq_ids, kv_head, pos_lo, pos_hi, delta, rope_theta,
+                        stream)
 
     def release(self, seq: int, stream=None) -> None:
         sp_release_seq(self.handle, seq, stream)

@@ -6,7 +6,7 @@ from __future__ import annotations
 
 import ctypes
 import os
-from ctypes import POINTER, c_char_p, c_int32, c_int64, c_size_t, c_void_p
+from ctypes import POINTER, c_char_p, c_double, c_int32, c_int64, c_size_t, c_void_p
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libsegpaged.so")
@@ -20,7 +20,7 @@ GLOBAL, LOCAL, RETRIEVAL = 0, 1, 2
 # Every symbol include/segpaged.h declares.
 EXPORTS = ("sp_required_bytes", "sp_cache_create", "sp_cache_destroy", "sp_set_policy",
            "sp_build_cache", "sp_append_kv", "sp_attention_prefill", "sp_attention_decode",
-           "sp_attention_decode_static_scratch",
+           "sp_attention_decode_static_scratch", "sp_rope_realign",
            "sp_release_seq", "sp_export_table", "sp_visible_count", "sp_seq_len",
            "sp_free_pages", "sp_count_prefill_pairs", "sp_count_decode_bytes",
            "sp_get_status", "sp_last_error")
@@ -67,6 +67,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "sp_attention_prefill": [P, c_int32, I32P, c_int32, I32P, P, P, P, P, P, P],
         "sp_attention_decode": [P, c_int32, I32P, c_int32, P, P, P, P],
         "sp_attention_decode_static_scratch": [P, c_int32, I32P, c_int32, P, P, P, P],
+        "sp_rope_realign": [P, c_int32, I32P, c_int32, c_int32, c_int64, c_int64, c_int64,
+                            c_double, P],
         "sp_release_seq": [P, c_int32, P],
         "sp_export_table": [P, c_int32, c_int32, c_int32, I32P, I32P, I32P, c_int32, P],
         "sp_visible_count": [P, c_int32, c_int32, c_int32, I64P, c_int32, I32P, P],

@@ -17,7 +17,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libsegpaged.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["sp_api.cu", "sp_storage.cu", "sp_decode.cu", "sp_prefill.cu", "sp_decode_static.cu"]
+SOURCES = ["sp_api.cu", "sp_storage.cu", "sp_decode.cu", "sp_prefill.cu", "sp_decode_static.cu",
+           "sp_rope.cu"]
 
 
 def nvcc() -> str:

@@ -511,6 +511,69 @@ sp_status sp_release_seq(sp_cache* c, int32_t seq, void* stream) {
     return SP_OK;
 }
 
+sp_status sp_rope_realign(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32_t n_seqs,
+                          int32_t kv_head, int64_t pos_lo, int64_t pos_hi, int64_t delta,
+                          double rope_theta, void* stream) {
+    if (!c) return fail(SP_ERR_INVALID_ARG, "null handle");
+    if (!valid_layer(c, layer)) return fail(SP_ERR_INVALID_ARG, "layer out of range");
+    sp_status s = check_seq_list(c, seq_ids, n_seqs);
+    if (s != SP_OK) return s;
+    if (kv_head < -1 || kv_head >= c->cfg.num_kv_heads) return fail(SP_ERR_INVALID_ARG, "kv_head out of range");
+    if (pos_lo < 0 || pos_hi < pos_lo) return fail(SP_ERR_INVALID_ARG, "need 0 <= pos_lo <= pos_hi");
+    if (!(rope_theta > 0.0) || !std::isfinite(rope_theta))
+        return fail(SP_ERR_INVALID_ARG, "rope_theta must be positive and finite");
+    if (delta < -(int64_t(1) << 40) || delta > (int64_t(1) << 40))
+        return fail(SP_ERR_INVALID_ARG, "delta out of range (|delta| <= 2^40)");
+    if (pos_lo == pos_hi || delta == 0) return SP_OK;   // nothing moves
+    std::unique_ptr<RopeParams> pp(new RopeParams());
+    RopeParams& p = *pp;
+    p.meta = c->meta;
+    p.geo = c->geo;
+    p.layer = layer;
+    p.pos_lo = pos_lo;
+    p.pos_hi = pos_hi;
+    const int d = c->cfg.head_dim;
+    const double two_pi = 6.283185307179586476925286766559;
+    for (int i = 0; i < d / 2; ++i) {
+        // angle delta * theta^(-2i/d), reduced in double before the cos / sin
+        const double ang = std::fmod((double)delta * std::pow(rope_theta, -2.0 * i / d), two_pi);
+        p.cs[i] = (float)std::cos(ang);
+        p.sn[i] = (float)std::sin(ang);
+    }
+    const int h0 = kv_head < 0 ? 0 : kv_head;
+    const int h1 = kv_head < 0 ? c->cfg.num_kv_heads : kv_head + 1;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // units in launches of at most kMaxRopeUnits, each with its page offsets
+    p.n_units = 0;
+    p.page_off[0] = 0;
+    auto flush = [&]() -> cudaError_t {
+        if (p.n_units == 0) return cudaSuccess;
+        cudaError_t e = launch_rope(c, p, st);
+        p.n_units = 0;
+        p.page_off[0] = 0;
+        return e;
+    };
+    for (int b = 0; b < n_seqs; ++b) {
+        const int32_t n = c->h_seqlen[(size_t)seq_ids[b] * c->cfg.num_layers + layer];
+        for (int h = h0; h < h1; ++h) {
+            const int32_t np = c->h_npages[unit_index(c, seq_ids[b], layer, h)];
+            if (np == 0) continue;
+            const int u = p.n_units++;
+            p.unit_seq[u] = seq_ids[b];
+            p.unit_head[u] = (int16_t)h;
+            p.unit_n[u] = n;
+            p.page_off[u + 1] = p.page_off[u] + np;
+            if (p.n_units == kMaxRopeUnits) {
+                cudaError_t e = flush();
+                if (e != cudaSuccess) return cuda_fail(e, "rope launch");
+            }
+        }
+    }
+    cudaError_t e = flush();
+    if (e != cudaSuccess) return cuda_fail(e, "rope launch");
+    return SP_OK;
+}
+
 sp_status sp_export_table(sp_cache* c, int32_t seq, int32_t layer, int32_t kv_head,
                           int32_t* npages, int32_t* page_ids, int32_t* slot_pos, int32_t cap,
                           void* stream) {

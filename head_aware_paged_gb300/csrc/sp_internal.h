@@ -66,6 +66,21 @@ struct DecodeParams {
     float scale_log2;            // log2(e) / sqrt(d)
 };
 
+// RoPE realignment of stored K rows (sp_rope.cu), one launch per call.
+constexpr int kMaxRopeUnits = 2048;   // (sequence, KV head) units in one rope launch
+struct RopeParams {
+    Meta meta;
+    Geo geo;
+    int32_t layer;
+    int32_t n_units;
+    int64_t pos_lo, pos_hi;       // rotate rows whose position is in [pos_lo, pos_hi)
+    float cs[64], sn[64];         // cos / sin of delta * theta^(-2i/d), i < d/2
+    int32_t unit_seq[kMaxRopeUnits];
+    int16_t unit_head[kMaxRopeUnits];
+    int32_t unit_n[kMaxRopeUnits];         // tokens the unit's (sequence, layer) holds
+    int32_t page_off[kMaxRopeUnits + 1];   // prefix of the units' page counts
+};
+
 struct Workspace {
     void* base;
     size_t bytes;
@@ -131,5 +146,6 @@ cudaError_t launch_export(const sp_cache* c, int seq, int layer, int h, int32_t*
 cudaError_t launch_decode_counts(const sp_cache* c, int seq, int layer, int h,
                                  const int64_t* pos, int n, int32_t* out, cudaStream_t s);
 cudaError_t launch_decode(const sp_cache* c, const DecodeParams& p, cudaStream_t s);
+cudaError_t launch_rope(const sp_cache* c, const RopeParams& p, cudaStream_t s);
 
 }  // namespace sp

@@ -189,6 +189,28 @@ sp_status sp_attention_decode_static_scratch(sp_cache* cache, int32_t layer,
                                              const void* q, void* out, float* lse,
                                              void* stream);
 
+/* RoPE realignment of reused keys (news summary, "Elastic Sparsity": the
+ * first recovery step is RoPE position alignment).  For every listed sequence
+ * and KV head kv_head (-1 = all KV heads) of `layer`, rotates in place every
+ * STORED K row whose token position p satisfies pos_lo <= p < pos_hi by
+ * `delta` positions of rotary embedding: with a_i = delta * rope_theta^(-2i/d)
+ * for i < d/2 (the "rotate half" pairing of element i with element i + d/2),
+ *     k'[i]       = k[i] cos a_i - k[i + d/2] sin a_i
+ *     k'[i + d/2] = k[i + d/2] cos a_i + k[i] sin a_i.
+ * The angles are formed and reduced modulo 2 pi in double precision on the
+ * host; the rotation runs in fp32 and rounds to bf16 (at most one bf16 ulp
+ * from the exact rotation of the stored value).  V and the recorded positions
+ * are not changed: a caller reusing KV computed at other positions stores it
+ * at its new positions and calls this with delta = new - old.  Rows outside
+ * [pos_lo, pos_hi), rows a policy does not store, and other heads are left
+ * untouched.  SP_ERR_INVALID_ARG for a bad list or head, pos_lo > pos_hi,
+ * rope_theta <= 0 or |delta| > 2^40.  The paper has no such entry point by
+ * name; this is its RoPE-alignment step applied to the paged layout. */
+sp_status sp_rope_realign(sp_cache* cache, int32_t layer, const int32_t* seq_ids,
+                          int32_t n_seqs, int32_t kv_head, int64_t pos_lo,
+                          int64_t pos_hi, int64_t delta, double rope_theta,
+                          void* stream);
+
 /* Return every page of `seq` (all layers) to the free stack and empty it; the
  * policy stays set. */
 sp_status sp_release_seq(sp_cache* cache, int32_t seq, void* stream);
