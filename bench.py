@@ -650,6 +650,74 @@ def run_op_rope(args):
             "clocks": clk}
 
 
+def run_op_pack(args):
+    """sp_pack_seq of Llama-3-8B-shaped sequences (32 layers x 8 KV heads x
+    32,768 tokens, the decode workload's policies): HBM-bound, every retained
+    row read from the pool and written to the packed buffer.  Also reports
+    the transfer-byte ratio dense / packed."""
+    import torch
+    from head_aware_paged_gb300 import Config, Policy, SegPagedCache, sp_pack_seq
+    wl = W.WORKLOADS["llama3_8b_decode_32k"]
+    B, n = 4, wl.seq_len
+    pols = W.policies(wl)
+    pages = 0
+    for row in pols:
+        for p_ in row:
+            pages += B * (-(-n // wl.page) + 1 if p_.kind == W.GLOBAL else
+                          -(-p_.sink // wl.page) + -(-p_.window // wl.page) + 2)
+    cfg = Config(num_layers=wl.layers, num_q_heads=wl.hq, num_kv_heads=wl.hkv, head_dim=wl.d,
+                 page_size=wl.page, max_seqs=B, max_seq_len=n, num_pages=pages + 16,
+                 max_tokens=n, max_batch=B)
+    c = SegPagedCache(cfg)
+    cp = [[Policy(p_.kind, p_.sink, p_.window) for p_ in row] for row in pols]
+    for b in range(B):
+        c.set_policy(b, cp)
+        for l in range(wl.layers):
+            k = W.normal((n, wl.hkv, wl.d), W.tensor_seed(0, "k", b, l), device="cuda")
+            v = W.normal((n, wl.hkv, wl.d), W.tensor_seed(0, "v", b, l), device="cuda")
+            c.build(b, l, k, v)
+            del k, v
+    torch.cuda.synchronize()
+    sizes = [sp_pack_seq(c.handle, b, None) for b in range(B)]
+    bufs = [c.pack(b) for b in range(B)]            # also the warm-up
+    torch.cuda.synchronize()
+    hdr = bufs[0][:88].cpu().numpy().view(np.int64)
+    payload = int(hdr[9])
+    dense = n * wl.layers * wl.hkv * 2 * wl.d * 2
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup):
+        for b in range(B):
+            sp_pack_seq(c.handle, b, bufs[b])
+    torch.cuda.synchronize()
+    peaks, src = load_peaks()
+    ms = []
+    for _ in range(args.steps):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for b in range(B):
+            sp_pack_seq(c.handle, b, bufs[b])
+        e1.record()
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    assert c.status() == 0
+    total = sum(ms)
+    moved = 2 * payload * B             # read from the pool + write to the buffer
+    gbs = moved * args.steps / (total / 1e3) / 1e9
+    peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    return {"metric": "Pack of trimmed per-head pages for transfer, GB/s moved (read + write)",
+            "op": "pack", "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total / args.steps, "higher_is_better": True,
+            "dtype": "bf16", "data": "synthetic (seeded N(0,1), pages' shapes)",
+            "config": {"workload": "llama3_8b_decode_32k policies, %d sequences x 32 layers x %d tokens" % (B, n),
+                       "packed_bytes_per_seq": sizes[0], "payload_bytes_per_seq": payload,
+                       "dense_kv_bytes_per_seq": dense, "transfer_ratio_dense_over_packed": dense / payload,
+                       "l2": "flushed between steps"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                         "frac": gbs / peak, "traffic": None, "kernel": "k_transfer",
+                         "peak_source": "%s hbm_gbs" % src}}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -661,13 +729,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-layers", type=int, default=0,
                     help="decode workload: run only the first N layers (profiling a small case)")
-    ap.add_argument("--op", default="", choices=["", "rope_realign"],
+    ap.add_argument("--op", default="", choices=["", "rope_realign", "pack"],
                     help="time one library operation instead of the attention step")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.op:
-        line = {"rope_realign": run_op_rope}[args.op](args)
+        line = {"rope_realign": run_op_rope, "pack": run_op_pack}[args.op](args)
         print(json.dumps(line), flush=True)
         return
     if args.impl == "reference":

@@ -149,6 +149,20 @@ def sp_rope_realign(handle, layer: int, seq_ids: Sequence[int], kv_head: int, po
                                  pos_lo, pos_hi, delta, float(rope_theta), _stream(stream)))
 
 
+def sp_pack_seq(handle, seq: int, dst: Optional[torch.Tensor], stream=None) -> int:
+    """Pack `seq` into dst (a 256-byte aligned device buffer); with dst None
+    only return the packed size in bytes."""
+    n = c_size_t()
+    nbytes = 0 if dst is None else dst.numel() * dst.element_size()
+    check(load().sp_pack_seq(handle, seq, _ptr(dst), nbytes, byref(n), _stream(stream)))
+    return n.value
+
+
+def sp_unpack_seq(handle, seq: int, src: torch.Tensor, stream=None) -> None:
+    check(load().sp_unpack_seq(handle, seq, _ptr(src), src.numel() * src.element_size(),
+                               _stream(stream)))
+
+
 def sp_release_seq(handle, seq: int, stream=None) -> None:
     check(load().sp_release_seq(handle, seq, _stream(stream)))
 
@@ -214,6 +228,7 @@ class SegPagedCache:
 
     def __init__(self, cfg: Config, device: str = "cuda"):
         self.cfg = cfg
+        self.device = device
         pool_b, meta_b, ws_b = sp_required_bytes(cfg)
         # 1024-byte alignment: torch's caching allocator returns 512-byte
         # aligned blocks, so over-allocate and offset.
@@ -291,6 +306,18 @@ class SegPagedCache:
         positions of rotary embedding (see sp_rope_realign in the C header)."""
         sp_rope_realign(self.handle, layer, seq_ids, kv_head, pos_lo, pos_hi, delta, rope_theta,
                         stream)
+
+    def pack(self, seq: int, stream=None) -> torch.Tensor:
+        """The packed transfer form of `seq` (header + trimmed rows) in a new
+        uint8 device tensor."""
+        n = sp_pack_seq(self.handle, seq, None)
+        _, buf = self._aligned(n, self.device)     # the view keeps its storage alive
+        sp_pack_seq(self.handle, seq, buf, stream)
+        return buf
+
+    def unpack(self, seq: int, buf: torch.Tensor, stream=None) -> None:
+        """Restore a packed sequence into the empty slot `seq`."""
+        sp_unpack_seq(self.handle, seq, buf, stream)
 
     def release(self, seq: int, stream=None) -> None:
         sp_release_seq(self.handle, seq, stream)

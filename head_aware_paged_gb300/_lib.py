@@ -20,7 +20,8 @@ GLOBAL, LOCAL, RETRIEVAL = 0, 1, 2
 # Every symbol include/segpaged.h declares.
 EXPORTS = ("sp_required_bytes", "sp_cache_create", "sp_cache_destroy", "sp_set_policy",
            "sp_build_cache", "sp_append_kv", "sp_attention_prefill", "sp_attention_decode",
-           "sp_attention_decode_static_scratch", "sp_rope_realign",
+           "sp_attention_decode_static_scratch", "sp_rope_realign", "sp_pack_seq",
+           "sp_unpack_seq",
            "sp_release_seq", "sp_export_table", "sp_visible_count", "sp_seq_len",
            "sp_free_pages", "sp_count_prefill_pairs", "sp_count_decode_bytes",
            "sp_get_status", "sp_last_error")
@@ -69,6 +70,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "sp_attention_decode_static_scratch": [P, c_int32, I32P, c_int32, P, P, P, P],
         "sp_rope_realign": [P, c_int32, I32P, c_int32, c_int32, c_int64, c_int64, c_int64,
                             c_double, P],
+        "sp_pack_seq": [P, c_int32, P, c_size_t, POINTER(c_size_t), P],
+        "sp_unpack_seq": [P, c_int32, P, c_size_t, P],
         "sp_release_seq": [P, c_int32, P],
         "sp_export_table": [P, c_int32, c_int32, c_int32, I32P, I32P, I32P, c_int32, P],
         "sp_visible_count": [P, c_int32, c_int32, c_int32, I64P, c_int32, I32P, P],

@@ -115,13 +115,18 @@ const int32_t* host_idx(const sp_cache* c, int seq, const UnitPol& u) {
 
 // Shared by build and append: validate lengths, check pool capacity against
 // the host mirror, then launch the allocator and the scatter kernel.
-sp_status write_tokens(sp_cache* c, int32_t layer, const int32_t* seqs, int32_t n_seqs,
-                       const int64_t* counts, const __nv_bfloat16* k, const __nv_bfloat16* v,
-                       int64_t row_stride, cudaStream_t stream) {
-    CallSeqs cs;
+// Allocate pages for `counts[b]` new tokens of each listed sequence in
+// `layer` (page-table build on the device) and advance the host mirror; the
+// caller then launches the kernel that fills the new slots.  cs / max_items
+// describe the call for that kernel.
+sp_status alloc_tokens(sp_cache* c, int32_t layer, const int32_t* seqs, int32_t n_seqs,
+                       const int64_t* counts, cudaStream_t stream, CallSeqs& cs,
+                       int64_t& max_items, int64_t& rows) {
     std::memset(&cs, 0, sizeof(cs));
     cs.n = n_seqs;
-    int64_t demand = 0, rows = 0, max_items = 0;
+    int64_t demand = 0;
+    rows = 0;
+    max_items = 0;
     for (int b = 0; b < n_seqs; ++b) {
         const int seq = seqs[b];
         const int64_t n_old = c->h_seqlen[(size_t)seq * c->cfg.num_layers + layer];
@@ -149,8 +154,6 @@ sp_status write_tokens(sp_cache* c, int32_t layer, const int32_t* seqs, int32_t 
     if (rows == 0) return SP_OK;
     cudaError_t e = launch_alloc(c, cs, layer, (int32_t)c->h_free, stream);
     if (e != cudaSuccess) return cuda_fail(e, "allocator launch");
-    e = launch_scatter(c, cs, layer, k, v, row_stride, max_items, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "scatter launch");
     c->h_free -= demand;
     for (int b = 0; b < n_seqs; ++b) {
         const int seq = seqs[b];
@@ -163,6 +166,18 @@ sp_status write_tokens(sp_cache* c, int32_t layer, const int32_t* seqs, int32_t 
                                                   c->cfg.page_size);
         }
     }
+    return SP_OK;
+}
+
+sp_status write_tokens(sp_cache* c, int32_t layer, const int32_t* seqs, int32_t n_seqs,
+                       const int64_t* counts, const __nv_bfloat16* k, const __nv_bfloat16* v,
+                       int64_t row_stride, cudaStream_t stream) {
+    CallSeqs cs;
+    int64_t max_items = 0, rows = 0;
+    sp_status s = alloc_tokens(c, layer, seqs, n_seqs, counts, stream, cs, max_items, rows);
+    if (s != SP_OK || rows == 0) return s;
+    cudaError_t e = launch_scatter(c, cs, layer, k, v, row_stride, max_items, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "scatter launch");
     return SP_OK;
 }
 
@@ -180,7 +195,53 @@ sp_status check_seq_list(const sp_cache* c, const int32_t* seq_ids, int32_t n_se
     return SP_OK;
 }
 
+// Rows a unit holding n tokens keeps (the retained set of the slot rules):
+// GLOBAL every token, LOCAL the sink and the newest ring's worth, RETRIEVAL
+// its listed positions below n.
+int64_t retained_rows(const UnitPol& u, const int32_t* idx, int64_t n, int P) {
+    if (n <= 0) return 0;
+    if (u.kind == kGlobal) return n;
+    if (u.kind == kLocal)
+        return std::min<int64_t>(n, u.sink) + std::min<int64_t>(std::max<int64_t>(n - u.sink, 0),
+                                                                (int64_t)u.ring * P);
+    return count_below(idx, u.n_idx, n);
+}
+
+// UnitPol of a LOCAL / GLOBAL / RETRIEVAL class, as sp_set_policy encodes it.
+UnitPol encode_unit(int64_t kind, int64_t sink, int64_t window, int32_t idx_off, int32_t n_idx,
+                    int P) {
+    UnitPol r{};
+    r.kind = (int32_t)kind;
+    if (kind == kLocal) {
+        r.sink = (int32_t)sink;
+        r.window = (int32_t)window;
+        r.ring = (int32_t)((window + P - 1) / P + 1);
+        r.sink_pages = (int32_t)((sink + P - 1) / P);
+    } else if (kind == kRetrieval) {
+        r.idx_off = idx_off;
+        r.n_idx = n_idx;
+    }
+    return r;
+}
+
+size_t align_to(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
 }  // namespace
+
+void* stage_acquire(sp_cache* c, size_t bytes, int* slot) {
+    if (bytes > c->stage_bytes) return nullptr;
+    const int si = c->stage_next;
+    c->stage_next = (si + 1) % sp_cache::kStaging;
+    if (cudaEventSynchronize(c->stage_ev[si]) != cudaSuccess) return nullptr;
+    *slot = si;
+    return c->stage_buf[si];
+}
+
+cudaError_t stage_copy(sp_cache* c, int slot, void* dst, size_t bytes, cudaStream_t s) {
+    cudaError_t e = cudaMemcpyAsync(dst, c->stage_buf[slot], bytes, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaEventRecord(c->stage_ev[slot], s);
+    return e;
+}
 
 sp_status fail(sp_status s, const std::string& msg) {
     g_last_error = msg;
@@ -286,8 +347,13 @@ sp_status sp_cache_create(const sp_config* cfg, void* pool, void* meta, void* ws
     // zero weight, so they must hold finite values).
     // pinned host staging ring for the prefill work list (host memory: the
     // device buffers stay the caller's)
+    // (also the header of a packed sequence, see sp_pack_seq)
+    c->stage_bytes = std::max((size_t)L.max_tiles * sizeof(int4),
+                              align_to(sizeof(PackHeader) + 8 * (size_t)cfg->num_layers +
+                                           sizeof(PackUnit) * (size_t)cfg->num_layers * cfg->num_kv_heads +
+                                           4 * (size_t)std::max(cfg->max_idx_per_seq, 1), 256));
     for (int i = 0; i < sp_cache::kStaging && e == cudaSuccess; ++i) {
-        e = cudaHostAlloc(reinterpret_cast<void**>(&c->stage_buf[i]), (size_t)L.max_tiles * sizeof(int4),
+        e = cudaHostAlloc(reinterpret_cast<void**>(&c->stage_buf[i]), c->stage_bytes,
                           cudaHostAllocDefault);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->stage_ev[i], cudaEventDisableTiming);
     }
@@ -571,6 +637,163 @@ sp_status sp_rope_realign(sp_cache* c, int32_t layer, const int32_t* seq_ids, in
     }
     cudaError_t e = flush();
     if (e != cudaSuccess) return cuda_fail(e, "rope launch");
+    return SP_OK;
+}
+
+sp_status sp_pack_seq(sp_cache* c, int32_t seq, void* dst, size_t dst_bytes, size_t* packed_bytes,
+                      void* stream) {
+    if (!c || !packed_bytes) return fail(SP_ERR_INVALID_ARG, "null argument");
+    if (!valid_seq(c, seq)) return fail(SP_ERR_INVALID_ARG, "sequence id out of range");
+    if (!c->h_policy_set[seq]) return fail(SP_ERR_INVALID_ARG, "sequence has no policy");
+    const int L = c->cfg.num_layers, H = c->cfg.num_kv_heads, d = c->cfg.head_dim;
+    const int P = c->cfg.page_size, U = L * H;
+    int64_t idx_total = 0;
+    for (int u = 0; u < U; ++u) {
+        const UnitPol& up = c->h_pol[unit_index(c, seq, u / H, u % H)];
+        if (up.kind == kRetrieval) idx_total += up.n_idx;
+    }
+    const size_t off_n = sizeof(PackHeader), off_units = off_n + 8 * (size_t)L;
+    const size_t off_idx = off_units + sizeof(PackUnit) * (size_t)U;
+    const size_t payload_off = align_to(off_idx + 4 * (size_t)idx_total, 256);
+    int slot = -1;
+    uint8_t* head = dst ? static_cast<uint8_t*>(stage_acquire(c, payload_off, &slot)) : nullptr;
+    std::vector<uint8_t> scratch;
+    if (!head) {                                       // size query, or a header too large to stage
+        if (dst && payload_off <= c->stage_bytes) return fail(SP_ERR_CUDA, "pinned staging buffer");
+        scratch.assign(payload_off, 0);
+        head = scratch.data();
+    } else {
+        std::memset(head, 0, payload_off);
+    }
+    PackHeader* ph = reinterpret_cast<PackHeader*>(head);
+    int64_t* nl = reinterpret_cast<int64_t*>(head + off_n);
+    PackUnit* pu = reinterpret_cast<PackUnit*>(head + off_units);
+    int32_t* pidx = reinterpret_cast<int32_t*>(head + off_idx);
+    int64_t row_off = 0, blk_off = 0, io = 0;
+    for (int l = 0; l < L; ++l) nl[l] = c->h_seqlen[(size_t)seq * L + l];
+    for (int u = 0; u < U; ++u) {
+        const UnitPol& up = c->h_pol[unit_index(c, seq, u / H, u % H)];
+        const int32_t* idx = host_idx(c, seq, up);
+        const int64_t rows = retained_rows(up, idx, nl[u / H], P);
+        pu[u] = PackUnit{up.kind, up.sink, up.window, up.kind == kRetrieval ? up.n_idx : 0, rows,
+                         row_off, blk_off};
+        if (up.kind == kRetrieval)
+            for (int k = 0; k < up.n_idx; ++k) pidx[io++] = idx[k];
+        row_off += rows;
+        blk_off += (rows + kTransferRows - 1) / kTransferRows;
+    }
+    const size_t payload_bytes = (size_t)row_off * 2 * d * 2;
+    *ph = PackHeader{kPackMagic, 1, L, H, d, P, U, idx_total, (int64_t)payload_off,
+                     (int64_t)payload_bytes, (int64_t)(payload_off + payload_bytes)};
+    *packed_bytes = payload_off + payload_bytes;
+    if (!dst) return SP_OK;                            // size query
+    if (dst_bytes < *packed_bytes) return fail(SP_ERR_INVALID_ARG, "dst smaller than the packed size");
+    if (reinterpret_cast<uintptr_t>(dst) & 255) return fail(SP_ERR_INVALID_ARG, "dst must be 256-byte aligned");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (slot >= 0) {
+        e = stage_copy(c, slot, dst, payload_off, st);  // asynchronous, from pinned memory
+    } else {
+        e = cudaMemcpyAsync(dst, head, payload_off, cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);   // the host header goes out of scope
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "pack header upload");
+    uint8_t* db = static_cast<uint8_t*>(dst);
+    TransferParams tp{};
+    tp.meta = c->meta;
+    tp.geo = c->geo;
+    tp.seq = seq;
+    tp.unpack = 0;
+    tp.n_units = U;
+    tp.total_blocks = blk_off;
+    tp.n_layer = reinterpret_cast<const int64_t*>(db + off_n);
+    tp.units = reinterpret_cast<const PackUnit*>(db + off_units);
+    tp.payload = reinterpret_cast<__nv_bfloat16*>(db + payload_off);
+    e = launch_transfer(c, tp, st);
+    if (e != cudaSuccess) return cuda_fail(e, "pack launch");
+    return SP_OK;
+}
+
+sp_status sp_unpack_seq(sp_cache* c, int32_t seq, const void* src, size_t src_bytes, void* stream) {
+    if (!c || !src) return fail(SP_ERR_INVALID_ARG, "null argument");
+    if (!valid_seq(c, seq)) return fail(SP_ERR_INVALID_ARG, "sequence id out of range");
+    if (reinterpret_cast<uintptr_t>(src) & 255) return fail(SP_ERR_INVALID_ARG, "src must be 256-byte aligned");
+    for (int l = 0; l < c->cfg.num_layers; ++l)
+        if (c->h_seqlen[(size_t)seq * c->cfg.num_layers + l] != 0)
+            return fail(SP_ERR_INVALID_ARG, "sequence holds tokens; release it first");
+    if (src_bytes < sizeof(PackHeader)) return fail(SP_ERR_INVALID_ARG, "src shorter than a header");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    PackHeader ph;
+    cudaError_t e = cudaMemcpyAsync(&ph, src, sizeof(ph), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "unpack header read");
+    const int L = c->cfg.num_layers, H = c->cfg.num_kv_heads, P = c->cfg.page_size;
+    const int U = L * H;
+    if (ph.magic != kPackMagic || ph.version != 1) return fail(SP_ERR_INVALID_ARG, "not a packed sequence");
+    if (ph.layers != L || ph.hkv != H || ph.head_dim != c->cfg.head_dim || ph.page_size != P ||
+        ph.n_units != U)
+        return fail(SP_ERR_INVALID_ARG, "packed sequence has another layer count, head count, "
+                                        "head_dim or page_size");
+    const size_t off_n = sizeof(PackHeader), off_units = off_n + 8 * (size_t)L;
+    const size_t off_idx = off_units + sizeof(PackUnit) * (size_t)U;
+    if (ph.idx_total < 0 || ph.payload_off != (int64_t)align_to(off_idx + 4 * (size_t)ph.idx_total, 256) ||
+        ph.total_bytes != ph.payload_off + ph.payload_bytes || (size_t)ph.total_bytes > src_bytes)
+        return fail(SP_ERR_INVALID_ARG, "packed header inconsistent with its size");
+    std::vector<uint8_t> head(ph.payload_off);
+    e = cudaMemcpyAsync(head.data(), src, head.size(), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "unpack header read");
+    const int64_t* nl = reinterpret_cast<const int64_t*>(head.data() + off_n);
+    const PackUnit* pu = reinterpret_cast<const PackUnit*>(head.data() + off_units);
+    const int32_t* pidx = reinterpret_cast<const int32_t*>(head.data() + off_idx);
+    // policies and capacity first: a refused unpack changes nothing
+    std::vector<sp_head_policy> pols(U);
+    int64_t io = 0, demand = 0, rows_total = 0, blocks = 0;
+    for (int u = 0; u < U; ++u) {
+        const PackUnit& x = pu[u];
+        if (x.kind < kGlobal || x.kind > kRetrieval || x.n_idx < 0 || io + x.n_idx > ph.idx_total)
+            return fail(SP_ERR_INVALID_ARG, "packed unit record out of range");
+        pols[u] = sp_head_policy{(int32_t)x.kind, (int32_t)x.sink, (int32_t)x.window,
+                                 (int32_t)x.n_idx, x.n_idx ? pidx + io : nullptr};
+        const int64_t n = nl[u / H];
+        if (n < 0 || n > c->cfg.max_seq_len) return fail(SP_ERR_INVALID_ARG, "packed length out of range");
+        const UnitPol r = encode_unit(x.kind, x.sink, x.window, 0, (int32_t)x.n_idx, P);
+        const int32_t* idx = x.kind == kRetrieval ? pidx + io : nullptr;
+        if (x.rows != retained_rows(r, idx, n, P) || x.row_off != rows_total || x.blk_off != blocks)
+            return fail(SP_ERR_INVALID_ARG, "packed unit layout does not follow its policy");
+        demand += unit_pages(r, idx, n, P);
+        rows_total += x.rows;
+        blocks += (x.rows + kTransferRows - 1) / kTransferRows;
+        io += x.n_idx;
+    }
+    if (ph.payload_bytes != rows_total * 2 * c->cfg.head_dim * 2)
+        return fail(SP_ERR_INVALID_ARG, "packed payload size does not match its units");
+    if (demand > c->h_free)
+        return fail(SP_ERR_OUT_OF_PAGES, "unpack needs " + std::to_string(demand) + " pages, " +
+                                             std::to_string(c->h_free) + " free");
+    sp_status s = sp_set_policy(c, seq, pols.data(), stream);
+    if (s != SP_OK) return s;
+    for (int l = 0; l < L; ++l) {
+        if (nl[l] == 0) continue;
+        CallSeqs cs;
+        int64_t max_items = 0, rows = 0;
+        const int64_t cnt = nl[l];
+        s = alloc_tokens(c, l, &seq, 1, &cnt, st, cs, max_items, rows);
+        if (s != SP_OK) return s;
+    }
+    const uint8_t* sb = static_cast<const uint8_t*>(src);
+    TransferParams tp{};
+    tp.meta = c->meta;
+    tp.geo = c->geo;
+    tp.seq = seq;
+    tp.unpack = 1;
+    tp.n_units = U;
+    tp.total_blocks = blocks;
+    tp.n_layer = reinterpret_cast<const int64_t*>(sb + off_n);
+    tp.units = reinterpret_cast<const PackUnit*>(sb + off_units);
+    tp.payload = const_cast<__nv_bfloat16*>(reinterpret_cast<const __nv_bfloat16*>(sb + ph.payload_off));
+    e = launch_transfer(c, tp, st);
+    if (e != cudaSuccess) return cuda_fail(e, "unpack launch");
     return SP_OK;
 }
 

@@ -81,6 +81,33 @@ struct RopeParams {
     int32_t page_off[kMaxRopeUnits + 1];   // prefix of the units' page counts
 };
 
+// Packed-sequence layout (sp_pack_seq / sp_unpack_seq).  The buffer starts
+// with PackHeader, then int64 n[layers] (tokens per layer), then
+// PackUnit[layers * hkv] in (layer, KV head) order, then the int32 retrieval
+// indices of every unit in the same order, then (at payload_off, 256-byte
+// aligned) the payload: for each unit its retained K rows then its V rows,
+// [rows][head_dim] bf16 each, in position order.
+constexpr int64_t kPackMagic = 0x3156504B50535053LL;   // "SPSPKPV1" little-endian
+constexpr int kTransferRows = 32;                        // rows per copy block
+struct PackHeader {
+    int64_t magic, version, layers, hkv, head_dim, page_size, n_units, idx_total,
+            payload_off, payload_bytes, total_bytes;
+};
+struct PackUnit {
+    int64_t kind, sink, window, n_idx, rows, row_off, blk_off;
+};
+struct TransferParams {
+    Meta meta;
+    Geo geo;
+    int32_t seq;
+    int32_t unpack;               // 0: pool -> payload, 1: payload -> pool
+    int32_t n_units;
+    int64_t total_blocks;
+    const int64_t* n_layer;       // device: tokens per layer (in the packed buffer)
+    const PackUnit* units;        // device: per-unit layout (in the packed buffer)
+    __nv_bfloat16* payload;       // device
+};
+
 struct Workspace {
     void* base;
     size_t bytes;
@@ -119,12 +146,19 @@ struct sp_cache {
     static constexpr int kStaging = 4;
     int4* stage_buf[kStaging] = {};
     cudaEvent_t stage_ev[kStaging] = {};
+    size_t stage_bytes = 0;                       // size of each buffer
     int stage_next = 0;
     bool prefill_checked[2][4] = {};             // [D == 128][log2(P) - 4]: attributes set
     ~sp_cache();
 };
 
 namespace sp {
+
+// Pinned staging ring (sp_api.cu): stage_acquire returns the next buffer once
+// the copy that last read it has run (nullptr if `bytes` does not fit);
+// stage_copy issues its asynchronous upload to `dst` and records its event.
+void* stage_acquire(sp_cache* c, size_t bytes, int* slot);
+cudaError_t stage_copy(sp_cache* c, int slot, void* dst, size_t bytes, cudaStream_t s);
 
 // Error plumbing (sp_api.cu).
 sp_status fail(sp_status s, const std::string& msg);
@@ -147,5 +181,6 @@ cudaError_t launch_decode_counts(const sp_cache* c, int seq, int layer, int h,
                                  const int64_t* pos, int n, int32_t* out, cudaStream_t s);
 cudaError_t launch_decode(const sp_cache* c, const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_rope(const sp_cache* c, const RopeParams& p, cudaStream_t s);
+cudaError_t launch_transfer(const sp_cache* c, const TransferParams& p, cudaStream_t s);
 
 }  // namespace sp

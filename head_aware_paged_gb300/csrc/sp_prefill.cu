@@ -764,11 +764,9 @@ sp_status prefill_impl(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32
     // previous copy has not run yet)
     const size_t n_items = cands.size();
     const size_t words = n_items + (grid + 1 + 3) / 4;
-    const int si = c->stage_next;
-    c->stage_next = (si + 1) % sp_cache::kStaging;
-    cudaError_t e = cudaEventSynchronize(c->stage_ev[si]);
-    if (e != cudaSuccess) return cuda_fail(e, "prefill staging buffer");
-    int4* buf = c->stage_buf[si];
+    int si = -1;
+    int4* buf = static_cast<int4*>(stage_acquire(c, words * sizeof(int4), &si));
+    if (!buf) return fail(SP_ERR_CUDA, "prefill staging buffer");
     int32_t* off = reinterpret_cast<int32_t*>(buf + n_items);
     size_t pos = 0;
     for (int g2 = 0; g2 < grid; ++g2) {
@@ -779,8 +777,7 @@ sp_status prefill_impl(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32
     p.items = c->ws.tiles;
     p.cta_off = reinterpret_cast<const int32_t*>(c->ws.tiles + n_items);
     p.n_items = (int32_t)n_items;
-    e = cudaMemcpyAsync(c->ws.tiles, buf, words * sizeof(int4), cudaMemcpyHostToDevice, stream);
-    if (e == cudaSuccess) e = cudaEventRecord(c->stage_ev[si], stream);
+    cudaError_t e = stage_copy(c, si, c->ws.tiles, words * sizeof(int4), stream);
     if (e != cudaSuccess) return cuda_fail(e, "prefill work list upload");
     CUtensorMap tq, tk, tv;
     std::string err;

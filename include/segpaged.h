@@ -211,6 +211,34 @@ sp_status sp_rope_realign(sp_cache* cache, int32_t layer, const int32_t* seq_ids
                           int64_t pos_hi, int64_t delta, double rope_theta,
                           void* stream);
 
+/* Pack / unpack one sequence for a prefill/decode-disaggregated transfer (news
+ * summary, "system gains": in the PD-separated setting only the tokens each
+ * head keeps travel, up to 6.3x fewer KV bytes).  The paper has no entry
+ * points by these names; these carry its trimmed per-head layout across.
+ *
+ * sp_pack_seq writes into the device buffer dst (256-byte aligned) a header
+ * (layer count, KV heads, head_dim, page_size, tokens per layer, every unit's
+ * policy and retrieval list, per-unit row offsets) followed by the payload:
+ * for each (layer, KV head) unit in order, its retained K rows then its
+ * retained V rows, [rows][head_dim] bf16 each, in position order (GLOBAL
+ * every token, LOCAL the sink then the newest ring's worth, RETRIEVAL its
+ * listed positions).  *packed_bytes receives the total size; with dst NULL the
+ * call only returns that size (no GPU work).  SP_ERR_INVALID_ARG if
+ * dst_bytes is smaller.  The header upload is synchronous; the copy runs on
+ * `stream`.
+ *
+ * sp_unpack_seq restores such a buffer into sequence slot `seq` of this cache,
+ * which must hold no tokens and have the same layer count, KV heads, head_dim
+ * and page_size: it sets the packed policy, allocates pages for every layer
+ * and copies the rows into their slots, so the tables, visible sets and
+ * attention results equal the source's.  It reads the header (synchronous),
+ * checks it against its own size and policies, and checks page capacity
+ * before changing anything (SP_ERR_INVALID_ARG / SP_ERR_OUT_OF_PAGES). */
+sp_status sp_pack_seq(sp_cache* cache, int32_t seq, void* dst, size_t dst_bytes,
+                      size_t* packed_bytes, void* stream);
+sp_status sp_unpack_seq(sp_cache* cache, int32_t seq, const void* src, size_t src_bytes,
+                        void* stream);
+
 /* Return every page of `seq` (all layers) to the free stack and empty it; the
  * policy stays set. */
 sp_status sp_release_seq(sp_cache* cache, int32_t seq, void* stream);
