@@ -718,6 +718,45 @@ def run_op_pack(args):
                          "peak_source": "%s hbm_gbs" % src}}
 
 
+def run_op_select(args):
+    """sp_select_heavy_hitters on one 32,768-token prompt (Hq 32 / Hkv 8,
+    d 128), observation window 64 rows, top-2048 (the retrieval heads of the
+    ragged mixed workload).  Work: two QK^T passes over every visible
+    (observation row, key) pair, 2 * 2d FLOP each."""
+    import torch
+    from head_aware_paged_gb300 import sp_select_heavy_hitters
+    n, n_obs, hq, hkv, d, topk = 32768, 64, 32, 8, 128, 2048
+    q = W.normal((n_obs, hq, d), 1, device="cuda")
+    k = W.normal((n, hkv, d), 2, scale=0.5, device="cuda")
+    flop = 2 * 2 * 2 * d * hq * sum(n - n_obs + oi + 1 for oi in range(n_obs))
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup):
+        sp_select_heavy_hitters(q, k, topk, 0)
+    torch.cuda.synchronize()
+    peaks, src = load_peaks()
+    ms = []
+    for _ in range(args.steps):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        sp_select_heavy_hitters(q, k, topk, 0)
+        e1.record()
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    total = sum(ms)
+    tf = flop * args.steps / (total / 1e3) / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    return {"metric": "Heavy-hitter retrieval selection, TFLOP/s over visible (row, key) pairs",
+            "op": "select", "value": tf, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total / args.steps, "higher_is_better": True,
+            "dtype": "bf16", "data": "synthetic (seeded N(0,1), K x 0.5)",
+            "config": {"workload": "one prompt n=%d, n_obs=%d, Hq %d / Hkv %d, d %d, top-%d" % (n, n_obs, hq, hkv, d, topk),
+                       "flop_per_call": flop, "l2": "flushed between calls"},
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tf / peak, "traffic": None, "kernel": "k_hh_tile (mma.sync)",
+                         "peak_source": "%s bf16_tflops" % src}}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -729,13 +768,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-layers", type=int, default=0,
                     help="decode workload: run only the first N layers (profiling a small case)")
-    ap.add_argument("--op", default="", choices=["", "rope_realign", "pack"],
+    ap.add_argument("--op", default="", choices=["", "rope_realign", "pack", "select"],
                     help="time one library operation instead of the attention step")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.op:
-        line = {"rope_realign": run_op_rope, "pack": run_op_pack}[args.op](args)
+        line = {"rope_realign": run_op_rope, "pack": run_op_pack, "select": run_op_select}[args.op](args)
         print(json.dumps(line), flush=True)
         return
     if args.impl == "reference":

@@ -163,6 +163,28 @@ def sp_unpack_seq(handle, seq: int, src: torch.Tensor, stream=None) -> None:
                                _stream(stream)))
 
 
+def sp_select_heavy_hitters(q_obs: torch.Tensor, k: torch.Tensor, topk: int, recent: int = 0,
+                            want_scores: bool = False, stream=None):
+    """Heavy-hitter retrieval selection on dense q_obs [n_obs, Hq, d] and k
+    [n, Hkv, d] (bf16, on the device).  Returns (idx [Hkv, topk + recent]
+    int32 padded with -1, counts [Hkv] int32, scores [Hkv, n] fp32 or None)."""
+    n_obs, hq, d = q_obs.shape
+    n, hkv, _ = k.shape
+    nbytes = c_size_t()
+    check(load().sp_select_workspace_bytes(n_obs, n, hq, hkv, byref(nbytes)))
+    ws = torch.empty(nbytes.value + 256, dtype=torch.uint8, device=k.device)
+    off = (-ws.data_ptr()) % 256
+    idx = torch.empty(hkv, topk + recent, dtype=torch.int32, device=k.device)
+    counts = torch.empty(hkv, dtype=torch.int32, device=k.device)
+    scores = torch.empty(hkv, n, dtype=torch.float32, device=k.device) if want_scores else None
+    check(load().sp_select_heavy_hitters(
+        _ptr(q_obs), n_obs, _ptr(k), n, hq, hkv, d, topk, recent,
+        ctypes.cast(idx.data_ptr(), ctypes.POINTER(c_int32)),
+        ctypes.cast(counts.data_ptr(), ctypes.POINTER(c_int32)),
+        _ptr(scores), c_void_p(ws.data_ptr() + off), nbytes.value, _stream(stream)))
+    return idx, counts, scores
+
+
 def sp_release_seq(handle, seq: int, stream=None) -> None:
     check(load().sp_release_seq(handle, seq, _stream(stream)))
 

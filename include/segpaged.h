@@ -211,6 +211,34 @@ sp_status sp_rope_realign(sp_cache* cache, int32_t layer, const int32_t* seq_ids
                           int64_t pos_hi, int64_t delta, double rope_theta,
                           void* stream);
 
+/* On-device retrieval selection, heavy hitters (runtime article section 2:
+ * retrieval heads see "the top-p important tokens"; section 5 measures an
+ * H2O heavy-hitter decode scenario).  No cache is involved: run it on the
+ * prompt's dense q / k before setting a RETRIEVAL(I) policy.
+ *   q_obs [n_obs][num_q_heads][head_dim] bf16: the observation rows, the last
+ *         n_obs query rows of the prompt (positions n - n_obs .. n - 1);
+ *   k     [n][num_kv_heads][head_dim] bf16: the prompt's keys (positions 0..n-1).
+ * For KV head h the score of key j is the causal softmax probability
+ * (scale 1/sqrt(head_dim), visible keys j <= position of the row) summed over
+ * h's query heads (grouped-query attention, query head q belongs to KV head
+ * q / (num_q_heads / num_kv_heads)) and over the observation rows.  The
+ * selection of head h is the topk highest scores among keys j < n - recent
+ * (ties: lower j first), then the recent window n - recent .. n - 1, all in
+ * ascending order.
+ * Outputs (device): idx [num_kv_heads][topk + recent] int32, row h holding
+ * min(topk, n - recent) + min(recent, n) indices followed by -1; counts
+ * [num_kv_heads] int32 (nullable); scores [num_kv_heads][n] fp32 (nullable).
+ * workspace: device scratch of sp_select_workspace_bytes(...) bytes, 256-byte
+ * aligned.  Asynchronous on `stream`.  The paper has no entry point by this
+ * name; it is the selection step its retrieval heads assume. */
+sp_status sp_select_workspace_bytes(int32_t n_obs, int32_t n, int32_t num_q_heads,
+                                    int32_t num_kv_heads, size_t* bytes);
+sp_status sp_select_heavy_hitters(const void* q_obs, int32_t n_obs, const void* k, int32_t n,
+                                  int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                  int32_t topk, int32_t recent, int32_t* idx, int32_t* counts,
+                                  float* scores, void* workspace, size_t workspace_bytes,
+                                  void* stream);
+
 /* Pack / unpack one sequence for a prefill/decode-disaggregated transfer (news
  * summary, "system gains": in the PD-separated setting only the tokens each
  * head keeps travel, up to 6.3x fewer KV bytes).  The paper has no entry
