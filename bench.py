@@ -247,14 +247,18 @@ class PrefillStep:
         return run_rows(n2), qf, kf, vf, pt
 
 
+FP8_SCALE = 5.6 / 448.0
+
+
 class DecodeStep:
     """Llama-3-8B-shaped decode: per layer, append one token per sequence and
     decode the batch; one step = all layers."""
 
-    def __init__(self, wl, device="cuda", layers=None):
+    def __init__(self, wl, device="cuda", layers=None, fp8=False):
         import torch
-        from head_aware_paged_gb300 import Config, Policy, SegPagedCache
+        from head_aware_paged_gb300 import KV_BF16, KV_FP8, Config, Policy, SegPagedCache
         self.wl = wl
+        self.fp8 = fp8
         self.layers = layers or wl.layers
         B, n = wl.seqs, wl.seq_len
         pols = W.policies(wl)[:self.layers]
@@ -269,8 +273,13 @@ class DecodeStep:
                     pages += B * ((p.sink + wl.page - 1) // wl.page + (p.window + wl.page - 1) // wl.page + 1)
         self.cfg = Config(num_layers=self.layers, num_q_heads=wl.hq, num_kv_heads=wl.hkv,
                           head_dim=wl.d, page_size=wl.page, max_seqs=B, max_seq_len=n + steps_cap,
-                          num_pages=pages + 16, max_tokens=max(n, B), max_batch=B)
+                          num_pages=pages + 16, max_tokens=max(n, B), max_batch=B,
+                          kv_dtype=KV_FP8 if fp8 else KV_BF16)
         self.cache = SegPagedCache(self.cfg)
+        if fp8:     # one scale for every channel: |x| up to 5.6 (N(0,1) data) maps inside +-448
+            sc = np.full((wl.hkv, wl.d), FP8_SCALE, np.float32)
+            for l in range(self.layers):
+                self.cache.set_kv_scales(l, sc, sc)
         cp = [[Policy(p.kind, p.sink, p.window) for p in row] for row in pols]
         for b in range(B):
             self.cache.set_policy(b, cp)
@@ -355,8 +364,10 @@ def run_ours(args, ws, rank):
     torch.cuda.init()
     wl = W.WORKLOADS[args.workload]
     decode = wl.decode_steps > 0 and wl.name.startswith("llama3_8b")
+    if args.kv_dtype == "fp8" and not decode:
+        raise SystemExit("--kv-dtype fp8 applies to the decode workload (prefill over FP8 history is not built)")
     if decode:
-        st = DecodeStep(wl, layers=args.decode_layers or None)
+        st = DecodeStep(wl, layers=args.decode_layers or None, fp8=args.kv_dtype == "fp8")
     else:
         layer = bench_layer(wl)
         st = PrefillStep(wl, W.policies(wl)[layer])
@@ -427,7 +438,7 @@ def run_ours(args, ws, rank):
         e2e = {"value": ws * st.work * e2e_steps * scale / (e2e_ms / 1e3), "unit": st.unit,
                "h2d_bytes_per_step": st.h2d_bytes, "d2h_bytes_per_step": st.d2h_bytes}
     else:
-        bytes_in = (st.qs.numel() + st.kn.numel() + st.vn.numel()) * 2 * st.layers
+        bytes_in = (st.qs.numel() + st.kn.numel() + st.vn.numel()) * 2 * st.layers   # bf16 inputs
         bytes_out = (st.out.numel() * 2 + st.lse.numel() * 4) * st.layers
         hq_ = st.qs.cpu().pin_memory()
         hk_ = st.kn.cpu().pin_memory()
@@ -464,7 +475,8 @@ def run_ours(args, ws, rank):
         achieved = float(np.mean(kern_work)) / (kern_avg_ms / 1e3) / 1e9
         peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": load_traffic("k_decode", wl.name),
+                "frac": achieved / peak,
+                "traffic": load_traffic("k_decode", wl.name + ("_fp8" if st.fp8 else "")),
                 "kernel": "k_decode", "peak_source": src + " hbm_gbs",
                 "algorithmic_bytes_per_launch": int(np.mean(kern_work)),
                 "avg_launch_ms": kern_avg_ms}
@@ -483,7 +495,9 @@ def run_ours(args, ws, rank):
         "metric": "SegPaged prefill TFLOP/s & decode visible-KV GB/s, % of GB300 roofline",
         "value": value, "unit": st.unit, "n_gpus": ws, "steps": n_steps, "warmup": args.warmup,
         "ms_per_step": total_ms / n_steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1), pages' shapes)",
+        "vs_baseline": None,
+        "dtype": "e4m3 K/V pages, f16 MMA" if decode and st.fp8 else "bf16",
+        "data": "synthetic (seeded N(0,1), pages' shapes)",
         "config": config_dict(wl, decode, st),
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": st.kernels_per_step * n_steps, "clocks": clk,
@@ -498,7 +512,11 @@ def config_dict(wl, decode, st):
     if decode:
         d.update({"layers": st.layers, "batch": wl.seqs, "cached_tokens": wl.seq_len,
                   "global_units": wl.n_global, "local": [wl.local_sink, wl.local_window],
-                  "step": "all layers: append 1 token/seq + split-KV decode"})
+                  "step": "all layers: append 1 token/seq + split-KV decode",
+                  "kv_dtype": "fp8_e4m3" if st.fp8 else "bf16"})
+        if st.fp8:
+            d["workload"] = wl.name + "_fp8"
+            d["kv_scales"] = "%.6g for every channel of K and V" % FP8_SCALE
     else:
         layer = bench_layer(wl)
         d.update({"seq_len": wl.seq_len, "layer": layer, "global_kv_heads_in_layer": sum(
@@ -681,7 +699,7 @@ def run_op_pack(args):
     sizes = [sp_pack_seq(c.handle, b, None) for b in range(B)]
     bufs = [c.pack(b) for b in range(B)]            # also the warm-up
     torch.cuda.synchronize()
-    hdr = bufs[0][:88].cpu().numpy().view(np.int64)
+    hdr = bufs[0][:96].cpu().numpy().view(np.int64)
     payload = int(hdr[9])
     dense = n * wl.layers * wl.hkv * 2 * wl.d * 2
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
@@ -768,6 +786,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-layers", type=int, default=0,
                     help="decode workload: run only the first N layers (profiling a small case)")
+    ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
+                    help="decode workload: page element type (fp8 = e4m3 codes with per-channel scales)")
     ap.add_argument("--op", default="", choices=["", "rope_realign", "pack", "select"],
                     help="time one library operation instead of the attention step")
     args = ap.parse_args()

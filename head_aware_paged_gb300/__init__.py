@@ -20,13 +20,14 @@ from ctypes import byref, c_int32, c_int64, c_size_t, c_void_p
 from dataclasses import dataclass
 from typing import List, Optional, Sequence
 
+import numpy as np
 import torch
 
-from ._lib import (EXPORTS, GLOBAL, LOCAL, RETRIEVAL, SegPagedError, SpConfig, SpHeadPolicy,
+from ._lib import (EXPORTS, GLOBAL, KV_BF16, KV_FP8, LOCAL, RETRIEVAL, SegPagedError, SpConfig, SpHeadPolicy,
                    check, i32_array, i64_array, load)
 
 __all__ = ["Config", "Policy", "SegPagedCache", "SegPagedError", "GLOBAL", "LOCAL",
-           "RETRIEVAL", "load", "EXPORTS"] + list(EXPORTS)
+           "RETRIEVAL", "KV_BF16", "KV_FP8", "load", "EXPORTS"] + list(EXPORTS)
 
 
 @dataclass
@@ -42,11 +43,12 @@ class Config:
     max_idx_per_seq: int = 0
     max_tokens: int = 8192
     max_batch: int = 1
+    kv_dtype: int = 0          # KV_BF16, or KV_FP8 (e4m3 pages with per-channel scales)
 
     def to_c(self) -> SpConfig:
         return SpConfig(self.num_layers, self.num_q_heads, self.num_kv_heads, self.head_dim,
                         self.page_size, self.max_seqs, self.max_seq_len, self.num_pages,
-                        self.max_idx_per_seq, self.max_tokens, self.max_batch)
+                        self.max_idx_per_seq, self.max_tokens, self.max_batch, self.kv_dtype)
 
 
 @dataclass
@@ -185,6 +187,15 @@ def sp_select_heavy_hitters(q_obs: torch.Tensor, k: torch.Tensor, topk: int, rec
     return idx, counts, scores
 
 
+def sp_set_kv_scales(handle, layer: int, k_scale, v_scale, stream=None) -> None:
+    """Per-channel FP8 scales of one layer: host float arrays [Hkv][d]."""
+    ks = np.ascontiguousarray(np.asarray(k_scale, dtype=np.float32).reshape(-1))
+    vs = np.ascontiguousarray(np.asarray(v_scale, dtype=np.float32).reshape(-1))
+    fp = ctypes.POINTER(ctypes.c_float)
+    check(load().sp_set_kv_scales(handle, layer, ks.ctypes.data_as(fp), vs.ctypes.data_as(fp),
+                                  _stream(stream)))
+
+
 def sp_release_seq(handle, seq: int, stream=None) -> None:
     check(load().sp_release_seq(handle, seq, _stream(stream)))
 
@@ -278,14 +289,17 @@ class SegPagedCache:
 
     # views of the page pool: [num_pages, page_size, head_dim] bf16 each
     def k_pool(self) -> torch.Tensor:
+        """K pages [num_pages][page_size][head_dim]: bf16, or uint8 e4m3 codes."""
         c = self.cfg
         half = c.num_pages * c.page_size * c.head_dim
-        return self.pool.view(torch.bfloat16)[:half].view(c.num_pages, c.page_size, c.head_dim)
+        dt = torch.uint8 if c.kv_dtype == KV_FP8 else torch.bfloat16
+        return self.pool.view(dt)[:half].view(c.num_pages, c.page_size, c.head_dim)
 
     def v_pool(self) -> torch.Tensor:
         c = self.cfg
         half = c.num_pages * c.page_size * c.head_dim
-        return self.pool.view(torch.bfloat16)[half:2 * half].view(c.num_pages, c.page_size, c.head_dim)
+        dt = torch.uint8 if c.kv_dtype == KV_FP8 else torch.bfloat16
+        return self.pool.view(dt)[half:2 * half].view(c.num_pages, c.page_size, c.head_dim)
 
     def set_policy(self, seq: int, policies, stream=None) -> None:
         flat = []
@@ -340,6 +354,9 @@ class SegPagedCache:
     def unpack(self, seq: int, buf: torch.Tensor, stream=None) -> None:
         """Restore a packed sequence into the empty slot `seq`."""
         sp_unpack_seq(self.handle, seq, buf, stream)
+
+    def set_kv_scales(self, layer: int, k_scale, v_scale, stream=None) -> None:
+        sp_set_kv_scales(self.handle, layer, k_scale, v_scale, stream)
 
     def release(self, seq: int, stream=None) -> None:
         sp_release_seq(self.handle, seq, stream)

@@ -16,12 +16,14 @@ STATUS_NAMES = {0: "SP_OK", 1: "SP_ERR_INVALID_ARG", 2: "SP_ERR_OUT_OF_PAGES",
                 3: "SP_ERR_UNSUPPORTED", 4: "SP_ERR_CUDA", 5: "SP_ERR_DEVICE_STATUS",
                 6: "SP_ERR_TIMEOUT"}
 GLOBAL, LOCAL, RETRIEVAL = 0, 1, 2
+KV_BF16, KV_FP8 = 0, 1
 
 # Every symbol include/segpaged.h declares.
 EXPORTS = ("sp_required_bytes", "sp_cache_create", "sp_cache_destroy", "sp_set_policy",
            "sp_build_cache", "sp_append_kv", "sp_attention_prefill", "sp_attention_decode",
            "sp_attention_decode_static_scratch", "sp_rope_realign", "sp_pack_seq",
            "sp_unpack_seq", "sp_select_workspace_bytes", "sp_select_heavy_hitters",
+           "sp_set_kv_scales",
            "sp_release_seq", "sp_export_table", "sp_visible_count", "sp_seq_len",
            "sp_free_pages", "sp_count_prefill_pairs", "sp_count_decode_bytes",
            "sp_get_status", "sp_last_error")
@@ -36,7 +38,7 @@ class SegPagedError(RuntimeError):
 class SpConfig(ctypes.Structure):
     _fields_ = [(n, c_int32) for n in (
         "num_layers", "num_q_heads", "num_kv_heads", "head_dim", "page_size", "max_seqs",
-        "max_seq_len", "num_pages", "max_idx_per_seq", "max_tokens", "max_batch")]
+        "max_seq_len", "num_pages", "max_idx_per_seq", "max_tokens", "max_batch", "kv_dtype")]
 
 
 class SpHeadPolicy(ctypes.Structure):
@@ -75,6 +77,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "sp_select_workspace_bytes": [c_int32, c_int32, c_int32, c_int32, POINTER(c_size_t)],
         "sp_select_heavy_hitters": [P, c_int32, P, c_int32, c_int32, c_int32, c_int32, c_int32,
                                     c_int32, I32P, I32P, P, P, c_size_t, P],
+        "sp_set_kv_scales": [P, c_int32, POINTER(ctypes.c_float), POINTER(ctypes.c_float), P],
         "sp_release_seq": [P, c_int32, P],
         "sp_export_table": [P, c_int32, c_int32, c_int32, I32P, I32P, I32P, c_int32, P],
         "sp_visible_count": [P, c_int32, c_int32, c_int32, I64P, c_int32, I32P, P],

@@ -24,7 +24,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct Layout {
     int32_t max_pages_unit = 0;
     size_t pol = 0, npages = 0, seqlen = 0, ptab = 0, idx = 0, fstack = 0, status = 0,
-           meta_total = 0;
+           scales = 0, meta_total = 0;
     size_t tiles = 0, tile_ctr = 0, part_o = 0, part_ml = 0, counters = 0, scratch = 0,
            ws_total = 0;
     int64_t max_tiles = 0, max_parts = 0, max_counter_units = 0, scratch_ints = 0;
@@ -54,6 +54,10 @@ sp_status check_config(const sp_config* c) {
         return fail(SP_ERR_UNSUPPORTED, "max_batch * num_kv_heads above 4096");
     if ((int64_t)c->num_layers * c->num_kv_heads > kMaxPolicyUnits)
         return fail(SP_ERR_UNSUPPORTED, "num_layers * num_kv_heads above 8192");
+    if (c->kv_dtype != SP_KV_BF16 && c->kv_dtype != SP_KV_FP8_E4M3)
+        return fail(SP_ERR_INVALID_ARG, "unknown kv_dtype");
+    if (c->kv_dtype == SP_KV_FP8_E4M3 && c->head_dim != 128)
+        return fail(SP_ERR_UNSUPPORTED, "FP8 pages need head_dim 128");
     return SP_OK;
 }
 
@@ -70,6 +74,8 @@ Layout make_layout(const sp_config* c) {
     L.idx = o;     o = align_up(o + S * (size_t)std::max(c->max_idx_per_seq, 1) * 4, 256);
     L.fstack = o;  o = align_up(o + (size_t)c->num_pages * 4, 256);
     L.status = o;  o = align_up(o + 64, 256);
+    // FP8 scales and their reciprocals: k, v, 1/k, 1/v, each [layers][hkv][d] fp32
+    L.scales = o;  o = align_up(o + 4 * (size_t)NL * H * c->head_dim * 4, 256);
     L.meta_total = o;
     const int group = c->num_q_heads / c->num_kv_heads;
     L.max_tiles = prefill_max_tiles(c);
@@ -84,7 +90,8 @@ Layout make_layout(const sp_config* c) {
     L.counters = o; o = align_up(o + L.max_counter_units * 4, 256);
     L.scratch = o;  o = align_up(o + L.scratch_ints * 4, 256);
     L.ws_total = o;
-    L.pool_total = 2 * (size_t)c->num_pages * c->page_size * c->head_dim * 2;
+    L.pool_total = 2 * (size_t)c->num_pages * c->page_size * c->head_dim *
+                   (c->kv_dtype == SP_KV_FP8_E4M3 ? 1 : 2);
     return L;
 }
 
@@ -255,14 +262,15 @@ sp_status cuda_fail(cudaError_t e, const char* what) {
 
 bool encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows, bool swizzle128,
-                    std::string* err) {
+                    std::string* err, bool bytes) {
     auto fn = get_encode();
     if (!fn) { *err = "cuTensorMapEncodeTiled unavailable (no CUDA driver)"; return false; }
     const cuuint64_t dims[2] = {inner, rows};
     const cuuint64_t strides[1] = {row_bytes};
     const cuuint32_t box[2] = {box_inner, box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+    const CUresult r = fn(map, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                          2, const_cast<void*>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -307,13 +315,15 @@ sp_status sp_cache_create(const sp_config* cfg, void* pool, void* meta, void* ws
     g.group = cfg->num_q_heads / cfg->num_kv_heads; g.d = cfg->head_dim; g.page = cfg->page_size;
     g.max_seqs = cfg->max_seqs; g.max_pages_unit = L.max_pages_unit;
     g.max_idx_per_seq = std::max(cfg->max_idx_per_seq, 1); g.num_pages = cfg->num_pages;
+    g.fp8 = cfg->kv_dtype == SP_KV_FP8_E4M3 ? 1 : 0;
     cudaError_t e = cudaGetDevice(&c->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
     if (e != cudaSuccess) { delete c; return cuda_fail(e, "device query"); }
     c->decode_ctas = std::min(c->num_sms, kMaxDecodeCtas);
     const size_t pool_half = (size_t)cfg->num_pages * cfg->page_size * cfg->head_dim;
+    // (FP8 pages: the same pointers address bytes; kernels cast them)
     c->kpool = static_cast<__nv_bfloat16*>(pool);
-    c->vpool = c->kpool + pool_half;
+    c->vpool = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(pool) + pool_half * (g.fp8 ? 1 : 2));
     uint8_t* mb = static_cast<uint8_t*>(meta);
     c->meta.pol = reinterpret_cast<UnitPol*>(mb + L.pol);
     c->meta.npages = reinterpret_cast<int32_t*>(mb + L.npages);
@@ -322,6 +332,14 @@ sp_status sp_cache_create(const sp_config* cfg, void* pool, void* meta, void* ws
     c->meta.idx = reinterpret_cast<int32_t*>(mb + L.idx);
     c->meta.fstack = reinterpret_cast<int32_t*>(mb + L.fstack);
     c->meta.status = reinterpret_cast<int32_t*>(mb + L.status);
+    {
+        const size_t nsc = (size_t)cfg->num_layers * cfg->num_kv_heads * cfg->head_dim;
+        float* sc = reinterpret_cast<float*>(mb + L.scales);
+        c->meta.kscale = sc;
+        c->meta.vscale = sc + nsc;
+        c->meta.kinv = sc + 2 * nsc;
+        c->meta.vinv = sc + 3 * nsc;
+    }
     uint8_t* wb = static_cast<uint8_t*>(ws);
     c->ws.base = ws; c->ws.bytes = L.ws_total;
     c->ws.tiles = reinterpret_cast<int4*>(wb + L.tiles); c->ws.max_tiles = L.max_tiles;
@@ -335,10 +353,14 @@ sp_status sp_cache_create(const sp_config* cfg, void* pool, void* meta, void* ws
     c->ws.scratch_ints = L.scratch_ints;
     std::string err;
     const uint64_t rows = (uint64_t)cfg->num_pages * cfg->page_size;
-    if (!encode_tmap_2d(&c->tm_kpool, c->kpool, cfg->head_dim, rows, cfg->head_dim * 2, 64,
-                        cfg->page_size, true, &err) ||
-        !encode_tmap_2d(&c->tm_vpool, c->vpool, cfg->head_dim, rows, cfg->head_dim * 2, 64,
-                        cfg->page_size, true, &err)) {
+    // bf16: boxes of 64 elements (one 128-byte swizzle row); FP8: a 128-element
+    // row is 128 bytes, one swizzle row
+    const uint32_t box = g.fp8 ? (uint32_t)cfg->head_dim : 64u;
+    const uint64_t rowb = (uint64_t)cfg->head_dim * (g.fp8 ? 1 : 2);
+    if (!encode_tmap_2d(&c->tm_kpool, c->kpool, cfg->head_dim, rows, rowb, box,
+                        cfg->page_size, true, &err, g.fp8) ||
+        !encode_tmap_2d(&c->tm_vpool, c->vpool, cfg->head_dim, rows, rowb, box,
+                        cfg->page_size, true, &err, g.fp8)) {
         delete c;
         return fail(SP_ERR_CUDA, err);
     }
@@ -362,6 +384,10 @@ sp_status sp_cache_create(const sp_config* cfg, void* pool, void* meta, void* ws
     if (e == cudaSuccess) e = cudaMemset(ws, 0, L.ws_total);
     if (e == cudaSuccess) e = cudaMemset(pool, 0, L.pool_total);
     if (e == cudaSuccess) e = launch_init_meta(c, 0);
+    if (e == cudaSuccess) {   // FP8 scales and reciprocals start at 1
+        const std::vector<float> ones(4 * (size_t)cfg->num_layers * cfg->num_kv_heads * cfg->head_dim, 1.f);
+        e = cudaMemcpy(c->meta.kscale, ones.data(), ones.size() * 4, cudaMemcpyHostToDevice);
+    }
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) { delete c; return cuda_fail(e, "cache initialisation"); }
     const size_t units = (size_t)cfg->max_seqs * cfg->num_layers * cfg->num_kv_heads;
@@ -513,6 +539,11 @@ sp_status sp_attention_prefill(sp_cache* c, int32_t layer, const int32_t* seq_id
             return fail(SP_ERR_INVALID_ARG, "chunk would pass max_seq_len");
     }
     if (cu_q[n_seqs] > c->cfg.max_tokens) return fail(SP_ERR_INVALID_ARG, "more rows than max_tokens");
+    if (c->geo.fp8)
+        for (int b = 0; b < n_seqs; ++b)
+            if (c->h_seqlen[(size_t)seq_ids[b] * c->cfg.num_layers + layer] != 0)
+                return fail(SP_ERR_UNSUPPORTED, "prefill over FP8 history pages is not built "
+                                                "(a chunk with no history is)");
     return prefill_impl(c, layer, seq_ids, n_seqs, cu_q, static_cast<const __nv_bfloat16*>(q),
                         static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v),
                         static_cast<__nv_bfloat16*>(out), lse, static_cast<cudaStream_t>(stream));
@@ -577,6 +608,35 @@ sp_status sp_release_seq(sp_cache* c, int32_t seq, void* stream) {
     return SP_OK;
 }
 
+sp_status sp_set_kv_scales(sp_cache* c, int32_t layer, const float* k_scale, const float* v_scale,
+                           void* stream) {
+    if (!c || !k_scale || !v_scale) return fail(SP_ERR_INVALID_ARG, "null argument");
+    if (!c->geo.fp8) return fail(SP_ERR_INVALID_ARG, "scales apply to FP8 pages only");
+    if (!valid_layer(c, layer)) return fail(SP_ERR_INVALID_ARG, "layer out of range");
+    for (int s = 0; s < c->cfg.max_seqs; ++s)
+        if (c->h_seqlen[(size_t)s * c->cfg.num_layers + layer] != 0)
+            return fail(SP_ERR_INVALID_ARG, "layer holds tokens; scales are fixed once a page is written");
+    const size_t n = (size_t)c->cfg.num_kv_heads * c->cfg.head_dim;
+    std::vector<float> ks(k_scale, k_scale + n), vs(v_scale, v_scale + n), ki(n), vi(n);
+    for (size_t i = 0; i < n; ++i) {
+        // f16 decode: the scale stays a normal f16 and 448 * scale stays finite
+        const float lo = 1.0f / 16384.0f, hi = 128.0f;
+        if (!(ks[i] >= lo && ks[i] <= hi) || !(vs[i] >= lo && vs[i] <= hi))
+            return fail(SP_ERR_INVALID_ARG, "scales must lie in [2^-14, 128]");
+        ki[i] = 1.0f / ks[i];     // fp32 reciprocals: the quantiser multiplies by these
+        vi[i] = 1.0f / vs[i];
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t off = (size_t)layer * n;
+    cudaError_t e = cudaMemcpyAsync(c->meta.kscale + off, ks.data(), n * 4, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(c->meta.vscale + off, vs.data(), n * 4, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(c->meta.kinv + off, ki.data(), n * 4, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(c->meta.vinv + off, vi.data(), n * 4, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "scale upload");
+    return SP_OK;
+}
+
 sp_status sp_rope_realign(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32_t n_seqs,
                           int32_t kv_head, int64_t pos_lo, int64_t pos_hi, int64_t delta,
                           double rope_theta, void* stream) {
@@ -590,6 +650,7 @@ sp_status sp_rope_realign(sp_cache* c, int32_t layer, const int32_t* seq_ids, in
         return fail(SP_ERR_INVALID_ARG, "rope_theta must be positive and finite");
     if (delta < -(int64_t(1) << 40) || delta > (int64_t(1) << 40))
         return fail(SP_ERR_INVALID_ARG, "delta out of range (|delta| <= 2^40)");
+    if (c->geo.fp8) return fail(SP_ERR_UNSUPPORTED, "RoPE realignment of FP8 pages is not built");
     if (pos_lo == pos_hi || delta == 0) return SP_OK;   // nothing moves
     std::unique_ptr<RopeParams> pp(new RopeParams());
     RopeParams& p = *pp;
@@ -682,9 +743,10 @@ sp_status sp_pack_seq(sp_cache* c, int32_t seq, void* dst, size_t dst_bytes, siz
         row_off += rows;
         blk_off += (rows + kTransferRows - 1) / kTransferRows;
     }
-    const size_t payload_bytes = (size_t)row_off * 2 * d * 2;
+    const size_t payload_bytes = (size_t)row_off * 2 * d * (c->geo.fp8 ? 1 : 2);
     *ph = PackHeader{kPackMagic, 1, L, H, d, P, U, idx_total, (int64_t)payload_off,
-                     (int64_t)payload_bytes, (int64_t)(payload_off + payload_bytes)};
+                     (int64_t)payload_bytes, (int64_t)(payload_off + payload_bytes),
+                     (int64_t)c->cfg.kv_dtype};
     *packed_bytes = payload_off + payload_bytes;
     if (!dst) return SP_OK;                            // size query
     if (dst_bytes < *packed_bytes) return fail(SP_ERR_INVALID_ARG, "dst smaller than the packed size");
@@ -708,7 +770,7 @@ sp_status sp_pack_seq(sp_cache* c, int32_t seq, void* dst, size_t dst_bytes, siz
     tp.total_blocks = blk_off;
     tp.n_layer = reinterpret_cast<const int64_t*>(db + off_n);
     tp.units = reinterpret_cast<const PackUnit*>(db + off_units);
-    tp.payload = reinterpret_cast<__nv_bfloat16*>(db + payload_off);
+    tp.payload = db + payload_off;
     e = launch_transfer(c, tp, st);
     if (e != cudaSuccess) return cuda_fail(e, "pack launch");
     return SP_OK;
@@ -731,9 +793,9 @@ sp_status sp_unpack_seq(sp_cache* c, int32_t seq, const void* src, size_t src_by
     const int U = L * H;
     if (ph.magic != kPackMagic || ph.version != 1) return fail(SP_ERR_INVALID_ARG, "not a packed sequence");
     if (ph.layers != L || ph.hkv != H || ph.head_dim != c->cfg.head_dim || ph.page_size != P ||
-        ph.n_units != U)
+        ph.n_units != U || ph.kv_dtype != c->cfg.kv_dtype)
         return fail(SP_ERR_INVALID_ARG, "packed sequence has another layer count, head count, "
-                                        "head_dim or page_size");
+                                        "head_dim, page_size or page type");
     const size_t off_n = sizeof(PackHeader), off_units = off_n + 8 * (size_t)L;
     const size_t off_idx = off_units + sizeof(PackUnit) * (size_t)U;
     if (ph.idx_total < 0 || ph.payload_off != (int64_t)align_to(off_idx + 4 * (size_t)ph.idx_total, 256) ||
@@ -766,7 +828,7 @@ sp_status sp_unpack_seq(sp_cache* c, int32_t seq, const void* src, size_t src_by
         blocks += (x.rows + kTransferRows - 1) / kTransferRows;
         io += x.n_idx;
     }
-    if (ph.payload_bytes != rows_total * 2 * c->cfg.head_dim * 2)
+    if (ph.payload_bytes != rows_total * 2 * c->cfg.head_dim * (c->geo.fp8 ? 1 : 2))
         return fail(SP_ERR_INVALID_ARG, "packed payload size does not match its units");
     if (demand > c->h_free)
         return fail(SP_ERR_OUT_OF_PAGES, "unpack needs " + std::to_string(demand) + " pages, " +
@@ -791,7 +853,7 @@ sp_status sp_unpack_seq(sp_cache* c, int32_t seq, const void* src, size_t src_by
     tp.total_blocks = blocks;
     tp.n_layer = reinterpret_cast<const int64_t*>(sb + off_n);
     tp.units = reinterpret_cast<const PackUnit*>(sb + off_units);
-    tp.payload = const_cast<__nv_bfloat16*>(reinterpret_cast<const __nv_bfloat16*>(sb + ph.payload_off));
+    tp.payload = const_cast<uint8_t*>(sb + ph.payload_off);
     e = launch_transfer(c, tp, st);
     if (e != cudaSuccess) return cuda_fail(e, "unpack launch");
     return SP_OK;
@@ -892,7 +954,7 @@ sp_status sp_count_decode_bytes(const sp_cache* c, int32_t layer, const int32_t*
             total += visible_count(u, host_idx(c, seq_ids[b], u), t[b]);
         }
     }
-    *bytes = total * 2 * c->cfg.head_dim * 2;
+    *bytes = total * 2 * c->cfg.head_dim * (c->geo.fp8 ? 1 : 2);   // K + V rows of the page type
     return SP_OK;
 }
 

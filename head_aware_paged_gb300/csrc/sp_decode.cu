@@ -33,31 +33,34 @@ constexpr int kConsumerWarps = 4;
 constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxGroup = 16;
 
-template <int D, int P>
+template <int D, int P, bool F8 = false>
 struct DecodeShape {
-    static constexpr int kHalves = D / 64;              // 128-byte column blocks per row
+    static constexpr int kElem = F8 ? 1 : 2;            // bytes per stored element
+    static constexpr int kHalves = D * kElem / 128;     // 128-byte column blocks per row
     static constexpr int kHalfBytes = P * 128;
     static constexpr int kTileBytes = kHalves * kHalfBytes;   // K (or V) of one page
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kStages = (160 * 1024 / kStageBytes) > 8 ? 8
-                                   : (160 * 1024 / kStageBytes) < 2 ? 2
-                                   : (160 * 1024 / kStageBytes);
+    static constexpr int kStageBudget = 160 * 1024;
+    static constexpr int kStages = (kStageBudget / kStageBytes) > 8 ? 8
+                                   : (kStageBudget / kStageBytes) < 2 ? 2
+                                   : (kStageBudget / kStageBytes);
     static constexpr int kMergeBytes = kConsumerWarps * kMaxGroup * (D + 2) * 4;
     static constexpr int kSmemBytes = kStages * kStageBytes + kMergeBytes
                                       + kStages * 16 /*full, empty*/ + kStages * 16 /*desc*/
                                       + 16 /*flags*/ + 32 * 16 /*producer batch*/
                                       + 1024 /*alignment slack*/;
+    static_assert(kSmemBytes <= 227 * 1024, "decode shared memory over the per-CTA limit");
 };
 
 __device__ __forceinline__ int64_t cta_of_item(int64_t x, int64_t T, int G) {
     return (x * G + G - 1) / T;
 }
 
-template <int D, int P>
+template <int D, int P, bool F8>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
 k_decode(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmK,
          const __grid_constant__ CUtensorMap tmV) {
-    using S = DecodeShape<D, P>;
+    using S = DecodeShape<D, P, F8>;
     constexpr int NST = S::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -196,16 +199,38 @@ k_decode(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtenso
         if (u != cur_u) {
             cur_u = u;
             const __nv_bfloat16* qb = p.q + ((int64_t)b * g.hq + h * group) * D;
-            #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const int col = kk * 16 + qc;
-                auto ld = [&](int r, int cc) -> uint32_t {
-                    return r < group ? *reinterpret_cast<const uint32_t*>(qb + (int64_t)r * D + cc) : 0u;
+            auto ld = [&](int r, int cc) -> uint32_t {
+                return r < group ? *reinterpret_cast<const uint32_t*>(qb + (int64_t)r * D + cc) : 0u;
+            };
+            if constexpr (F8) {
+                // q * k_scale as f16 (q . (code * s) = (q * s) . code), with
+                // the reduction index of step kk, lane quad j mapped to dims
+                // j*32 + kk*4 + {0,1 | 2,3}: one 32-bit word of a key's codes
+                // then feeds both halves of the B fragment
+                const float* ks = p.meta.kscale + ((int64_t)p.layer * g.hkv + h) * D;
+                auto ldq = [&](int r, int cc) -> uint32_t {
+                    const uint32_t w = ld(r, cc);
+                    const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162*>(&w);
+                    return pack_f16(__low2float(v2) * ks[cc], __high2float(v2) * ks[cc + 1]);
                 };
-                qa[kk][0] = ld(qr, col);
-                qa[kk][1] = ld(qr + 8, col);
-                qa[kk][2] = ld(qr, col + 8);
-                qa[kk][3] = ld(qr + 8, col + 8);
+                const int j = lane & 3;
+                #pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const int col = j * 32 + kk * 4;
+                    qa[kk][0] = ldq(qr, col);
+                    qa[kk][1] = ldq(qr + 8, col);
+                    qa[kk][2] = ldq(qr, col + 2);
+                    qa[kk][3] = ldq(qr + 8, col + 2);
+                }
+            } else {
+                #pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const int col = kk * 16 + qc;
+                    qa[kk][0] = ld(qr, col);
+                    qa[kk][1] = ld(qr + 8, col);
+                    qa[kk][2] = ld(qr, col + 8);
+                    qa[kk][3] = ld(qr + 8, col + 8);
+                }
             }
             m_run[0] = m_run[1] = -INFINITY;
             l_run[0] = l_run[1] = 0.f;
@@ -221,7 +246,26 @@ k_decode(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtenso
             if (key0 >= hi || key0 + 16 <= lo) continue;
             // S = Q K^T for 16 keys: two n-tiles of 8 keys
             float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            {
+            if constexpr (F8) {
+                // B fragments straight from the codes: lane (n, j) reads bytes
+                // j*32 .. j*32+31 of key n of each n-tile; word kk of them is
+                // dims j*32 + kk*4 .. +3 (e4m3 -> f16 is exact)
+                const uint8_t* tk = stages + s * S::kStageBytes;
+                const int j = lane & 3, n = lane >> 2;
+                #pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int key = key0 + nt * 8 + n;
+                    const uint4 c0 = *reinterpret_cast<const uint4*>(tk + sw128(key, 2 * j));
+                    const uint4 c1 = *reinterpret_cast<const uint4*>(tk + sw128(key, 2 * j + 1));
+                    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                    #pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        uint32_t b0, b1;
+                        f16x2x2_of_e4m3x4(w[kk], b0, b1);
+                        mma_f16_16816(sc[nt], qa[kk], b0, b1);
+                    }
+                }
+            } else {
                 const int mi = lane >> 3;
                 const uint32_t key = key0 + (lane & 7) + (mi >= 2 ? 8 : 0);
                 #pragma unroll
@@ -277,11 +321,43 @@ k_decode(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtenso
             }
             // O += P V: P from the S fragments (rows = heads, k = keys)
             uint32_t pa[4];
-            pa[0] = pack_bf16(sc[0][0], sc[0][1]);
-            pa[1] = pack_bf16(sc[0][2], sc[0][3]);
-            pa[2] = pack_bf16(sc[1][0], sc[1][1]);
-            pa[3] = pack_bf16(sc[1][2], sc[1][3]);
-            {
+            if constexpr (F8) {
+                pa[0] = pack_f16(sc[0][0], sc[0][1]);
+                pa[1] = pack_f16(sc[0][2], sc[0][3]);
+                pa[2] = pack_f16(sc[1][0], sc[1][1]);
+                pa[3] = pack_f16(sc[1][2], sc[1][3]);
+            } else {
+                pa[0] = pack_bf16(sc[0][0], sc[0][1]);
+                pa[1] = pack_bf16(sc[0][2], sc[0][3]);
+                pa[2] = pack_bf16(sc[1][0], sc[1][1]);
+                pa[3] = pack_bf16(sc[1][2], sc[1][3]);
+            }
+            if constexpr (F8) {
+                // The output dims of n-tile nt, column n are n*16 + nt, so lane
+                // (n, j) needs dims n*16 .. n*16+15 (chunk n) of keys 2j, 2j+1,
+                // 2j+8, 2j+9; byte interleaves pair consecutive keys per dim.
+                // V's scales are applied to the finished sums.
+                const uint8_t* tv = stages + s * S::kStageBytes + S::kTileBytes;
+                const int j = lane & 3, n = lane >> 2;
+                const uint4 r0 = *reinterpret_cast<const uint4*>(tv + sw128(key0 + 2 * j, n));
+                const uint4 r1 = *reinterpret_cast<const uint4*>(tv + sw128(key0 + 2 * j + 1, n));
+                const uint4 r8 = *reinterpret_cast<const uint4*>(tv + sw128(key0 + 2 * j + 8, n));
+                const uint4 r9 = *reinterpret_cast<const uint4*>(tv + sw128(key0 + 2 * j + 9, n));
+                const uint32_t a0[4] = {r0.x, r0.y, r0.z, r0.w}, a1[4] = {r1.x, r1.y, r1.z, r1.w};
+                const uint32_t a8[4] = {r8.x, r8.y, r8.z, r8.w}, a9[4] = {r9.x, r9.y, r9.z, r9.w};
+                #pragma unroll
+                for (int w = 0; w < 4; ++w) {            // dims n*16 + 4w .. +3: n-tiles 4w .. 4w+3
+                    uint32_t lo0, lo1, lo2, lo3, hi0, hi1, hi2, hi3;
+                    f16x2x2_of_e4m3x4(prmt(a0[w], a1[w], 0x5140u), lo0, lo1);   // bytes 0,1
+                    f16x2x2_of_e4m3x4(prmt(a0[w], a1[w], 0x7362u), lo2, lo3);   // bytes 2,3
+                    f16x2x2_of_e4m3x4(prmt(a8[w], a9[w], 0x5140u), hi0, hi1);
+                    f16x2x2_of_e4m3x4(prmt(a8[w], a9[w], 0x7362u), hi2, hi3);
+                    mma_f16_16816(o_acc[4 * w + 0], pa, lo0, hi0);
+                    mma_f16_16816(o_acc[4 * w + 1], pa, lo1, hi1);
+                    mma_f16_16816(o_acc[4 * w + 2], pa, lo2, hi2);
+                    mma_f16_16816(o_acc[4 * w + 3], pa, lo3, hi3);
+                }
+            } else {
                 const int mi = lane >> 3;
                 const uint32_t key = key0 + (lane & 7) + ((mi & 1) ? 8 : 0);
                 #pragma unroll
@@ -312,10 +388,20 @@ k_decode(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtenso
             const int row = qr + 8 * r;
             if (row < group) {
                 float* mo = merge_o + ((size_t)warp * kMaxGroup + row) * D;
-                #pragma unroll
-                for (int nt = 0; nt < D / 8; ++nt) {
-                    mo[nt * 8 + qc] = o_acc[nt][2 * r];
-                    mo[nt * 8 + qc + 1] = o_acc[nt][2 * r + 1];
+                if constexpr (F8) {       // column c of n-tile nt is dim c*16 + nt; times V's scale
+                    const float* vs = p.meta.vscale + ((int64_t)p.layer * g.hkv + h) * D;
+                    #pragma unroll
+                    for (int nt = 0; nt < D / 8; ++nt) {
+                        const int d0 = qc * 16 + nt, d1 = (qc + 1) * 16 + nt;
+                        mo[d0] = o_acc[nt][2 * r] * vs[d0];
+                        mo[d1] = o_acc[nt][2 * r + 1] * vs[d1];
+                    }
+                } else {
+                    #pragma unroll
+                    for (int nt = 0; nt < D / 8; ++nt) {
+                        mo[nt * 8 + qc] = o_acc[nt][2 * r];
+                        mo[nt * 8 + qc + 1] = o_acc[nt][2 * r + 1];
+                    }
                 }
                 if ((lane & 3) == 0) {
                     merge_ml[(warp * kMaxGroup + row) * 2] = m_run[r];
@@ -431,13 +517,13 @@ k_decode(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtenso
     }
 }
 
-template <int D, int P>
+template <int D, int P, bool F8 = false>
 cudaError_t launch_decode_t(const sp_cache* c, const DecodeParams& p, int grid, cudaStream_t s) {
-    using Sh = DecodeShape<D, P>;
-    cudaError_t e = cudaFuncSetAttribute(k_decode<D, P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    using Sh = DecodeShape<D, P, F8>;
+    cudaError_t e = cudaFuncSetAttribute(k_decode<D, P, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Sh::kSmemBytes);
     if (e != cudaSuccess) return e;
-    k_decode<D, P><<<grid, kDecodeThreads, Sh::kSmemBytes, s>>>(p, c->tm_kpool, c->tm_vpool);
+    k_decode<D, P, F8><<<grid, kDecodeThreads, Sh::kSmemBytes, s>>>(p, c->tm_kpool, c->tm_vpool);
     return cudaGetLastError();
 }
 
@@ -455,6 +541,14 @@ cudaError_t launch_decode(const sp_cache* c, const DecodeParams& p, cudaStream_t
     const int merge_cap = kConsumerWarps * kMaxGroup * c->geo.d / 2 / c->geo.group;
     if (grid > merge_cap) grid = merge_cap;
     const int D = c->geo.d, P = c->geo.page;
+    if (c->geo.fp8) {   // FP8 pages: head_dim 128 only (checked at create)
+        if (D != 128) return cudaErrorInvalidValue;
+        if (P == 16) return launch_decode_t<128, 16, true>(c, p, grid, s);
+        if (P == 32) return launch_decode_t<128, 32, true>(c, p, grid, s);
+        if (P == 64) return launch_decode_t<128, 64, true>(c, p, grid, s);
+        if (P == 128) return launch_decode_t<128, 128, true>(c, p, grid, s);
+        return cudaErrorInvalidValue;
+    }
 #define SP_DEC(DD, PP) if (D == DD && P == PP) return launch_decode_t<DD, PP>(c, p, grid, s);
     SP_DEC(64, 16) SP_DEC(64, 32) SP_DEC(64, 64) SP_DEC(64, 128)
     SP_DEC(128, 16) SP_DEC(128, 32) SP_DEC(128, 64) SP_DEC(128, 128)

@@ -27,12 +27,17 @@ struct Meta {
     int32_t* idx;        // [max_seqs][max_idx_per_seq]
     int32_t* fstack;     // [num_pages] free-page stack
     int32_t* status;     // [8]: 0 = status word, 1 = stack top (debug mirror)
+    float* kscale;       // FP8 pages: [layers][hkv][d] per-channel scales of K
+    float* vscale;       //            ... of V
+    float* kinv;         //            fp32 reciprocals used to quantise
+    float* vinv;
 };
 
 // Geometry every kernel needs.
 struct Geo {
     int32_t layers, hq, hkv, group, d, page, max_seqs, max_pages_unit,
             max_idx_per_seq, num_pages;
+    int32_t fp8;         // pages hold e4m3 codes (1 byte) instead of bf16
     __host__ __device__ int64_t unit_row(int seq, int layer, int h) const {
         return ((int64_t)seq * layers + layer) * hkv + h;
     }
@@ -86,12 +91,13 @@ struct RopeParams {
 // PackUnit[layers * hkv] in (layer, KV head) order, then the int32 retrieval
 // indices of every unit in the same order, then (at payload_off, 256-byte
 // aligned) the payload: for each unit its retained K rows then its V rows,
-// [rows][head_dim] bf16 each, in position order.
+// [rows][head_dim] elements of the page type (bf16, or e4m3 bytes), in
+// position order.
 constexpr int64_t kPackMagic = 0x3156504B50535053LL;   // "SPSPKPV1" little-endian
 constexpr int kTransferRows = 32;                        // rows per copy block
 struct PackHeader {
     int64_t magic, version, layers, hkv, head_dim, page_size, n_units, idx_total,
-            payload_off, payload_bytes, total_bytes;
+            payload_off, payload_bytes, total_bytes, kv_dtype;
 };
 struct PackUnit {
     int64_t kind, sink, window, n_idx, rows, row_off, blk_off;
@@ -105,7 +111,7 @@ struct TransferParams {
     int64_t total_blocks;
     const int64_t* n_layer;       // device: tokens per layer (in the packed buffer)
     const PackUnit* units;        // device: per-unit layout (in the packed buffer)
-    __nv_bfloat16* payload;       // device
+    uint8_t* payload;             // device
 };
 
 struct Workspace {
@@ -165,7 +171,7 @@ sp_status fail(sp_status s, const std::string& msg);
 sp_status cuda_fail(cudaError_t e, const char* what);
 bool encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows,
-                    bool swizzle128, std::string* err);
+                    bool swizzle128, std::string* err, bool bytes = false);
 
 // Launchers (return the launch's cudaError_t).
 cudaError_t launch_init_meta(const sp_cache* c, cudaStream_t s);

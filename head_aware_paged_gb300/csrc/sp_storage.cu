@@ -102,6 +102,23 @@ k_alloc(Meta m, Geo g, CallSeqs cs, int layer, int32_t top) {
     if (threadIdx.x == 0) m.status[1] = top - total;
 }
 
+// 8 bf16 values (one 16-byte vector) -> 8 e4m3 codes of x * inv[i] (fp32
+// product, then round to nearest even, saturated at +-448), in element order.
+__device__ __forceinline__ uint2 quant_e4m3x8(int4 x, const float* inv) {
+    const uint32_t w[4] = {(uint32_t)x.x, (uint32_t)x.y, (uint32_t)x.z, (uint32_t)x.w};
+    uint32_t out[2] = {0u, 0u};
+    #pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 p2 = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
+        const float lo = __low2float(p2) * __ldg(inv + 2 * e);
+        const float hi = __high2float(p2) * __ldg(inv + 2 * e + 1);
+        uint16_t code;   // first operand goes to the upper byte
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(code) : "f"(hi), "f"(lo));
+        out[e >> 1] |= (uint32_t)code << (16 * (e & 1));
+    }
+    return make_uint2(out[0], out[1]);
+}
+
 // Copy the retained rows of each unit into its pages (16-byte vectors).
 __global__ void __launch_bounds__(256)
 k_scatter(Meta m, Geo g, CallSeqs cs, int layer, const __nv_bfloat16* __restrict__ k,
@@ -131,8 +148,19 @@ k_scatter(Meta m, Geo g, CallSeqs cs, int layer, const __nv_bfloat16* __restrict
         if (page < 0 || page >= g.num_pages) { atomicOr(m.status, kStatusBadPage); continue; }
         const int64_t src = (cs.row0[b] + (t - n_old)) * row_stride + (int64_t)h * g.d + c * 8;
         const int64_t dst = ((int64_t)page * g.page + us % g.page) * g.d + c * 8;
-        *reinterpret_cast<int4*>(kpool + dst) = __ldg(reinterpret_cast<const int4*>(k + src));
-        *reinterpret_cast<int4*>(vpool + dst) = __ldg(reinterpret_cast<const int4*>(v + src));
+        const int4 kv = __ldg(reinterpret_cast<const int4*>(k + src));
+        const int4 vv = __ldg(reinterpret_cast<const int4*>(v + src));
+        if (!g.fp8) {
+            *reinterpret_cast<int4*>(kpool + dst) = kv;
+            *reinterpret_cast<int4*>(vpool + dst) = vv;
+        } else {
+            // e4m3 codes of x * (1 / scale), channel by channel (8 bytes per side)
+            const int64_t so = ((int64_t)layer * g.hkv + h) * g.d + c * 8;
+            uint8_t* kp = reinterpret_cast<uint8_t*>(kpool) + dst;
+            uint8_t* vp = reinterpret_cast<uint8_t*>(vpool) + dst;
+            *reinterpret_cast<uint2*>(kp) = quant_e4m3x8(kv, m.kinv + so);
+            *reinterpret_cast<uint2*>(vp) = quant_e4m3x8(vv, m.vinv + so);
+        }
     }
 }
 

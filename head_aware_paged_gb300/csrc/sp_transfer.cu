@@ -8,7 +8,8 @@
 // a header in front of it (written by the host) records the layout, the
 // policies and per-unit row and block offsets.  One kernel copies in either
 // direction between the page pool and the payload; it is HBM-bound
-// (2 * 2d bytes moved per retained token per head, read + write).
+// (2 * 2d bytes per retained token per head and side, read + write; half
+// that for FP8 pages).
 #include "sp_device.cuh"
 #include "sp_internal.h"
 
@@ -35,10 +36,11 @@ __device__ __forceinline__ void row_slot(const UnitPol& u, const int32_t* idx, i
 }
 
 __global__ void __launch_bounds__(256)
-k_transfer(const __grid_constant__ TransferParams p, __nv_bfloat16* kpool, __nv_bfloat16* vpool) {
+k_transfer(const __grid_constant__ TransferParams p, uint8_t* kpool, uint8_t* vpool) {
     const Geo& g = p.geo;
-    const int D = g.d, P = g.page;
-    const int vec = D / 8;                             // 16-byte chunks per row
+    const int P = g.page;
+    const int row_bytes = g.d * (g.fp8 ? 1 : 2);
+    const int vec = row_bytes / 16;                    // 16-byte chunks per row
     for (int64_t blk = blockIdx.x; blk < p.total_blocks; blk += gridDim.x) {
         int a = 0, z = p.n_units - 1;                  // unit with blk_off[u] <= blk < blk_off[u+1]
         while (a < z) {
@@ -55,8 +57,8 @@ k_transfer(const __grid_constant__ TransferParams p, __nv_bfloat16* kpool, __nv_
         const int32_t rows = (int32_t)un.rows;
         const int32_t r0 = (int32_t)(blk - un.blk_off) * kTransferRows;
         const int32_t nr = min(kTransferRows, rows - r0);
-        __nv_bfloat16* kblk = p.payload + 2 * un.row_off * D;     // the unit's K rows
-        __nv_bfloat16* vblk = kblk + (int64_t)rows * D;           // then its V rows
+        uint8_t* kblk = p.payload + 2 * un.row_off * row_bytes;   // the unit's K rows
+        uint8_t* vblk = kblk + (int64_t)rows * row_bytes;           // then its V rows
         for (int w = threadIdx.x; w < nr * vec * 2; w += blockDim.x) {
             const int kv = w / (nr * vec);             // 0 = K, 1 = V
             const int rem = w - kv * nr * vec;
@@ -69,8 +71,8 @@ k_transfer(const __grid_constant__ TransferParams p, __nv_bfloat16* kpool, __nv_
                 atomicOr(p.meta.status, kStatusBadPage);
                 continue;
             }
-            __nv_bfloat16* pool = (kv ? vpool : kpool) + ((int64_t)phys * P + slot % P) * D + c * 8;
-            __nv_bfloat16* pay = (kv ? vblk : kblk) + (int64_t)r * D + c * 8;
+            uint8_t* pool = (kv ? vpool : kpool) + ((int64_t)phys * P + slot % P) * row_bytes + c * 16;
+            uint8_t* pay = (kv ? vblk : kblk) + (int64_t)r * row_bytes + c * 16;
             if (p.unpack) *reinterpret_cast<uint4*>(pool) = *reinterpret_cast<const uint4*>(pay);
             else *reinterpret_cast<uint4*>(pay) = *reinterpret_cast<const uint4*>(pool);
         }
@@ -83,7 +85,8 @@ cudaError_t launch_transfer(const sp_cache* c, const TransferParams& p, cudaStre
     if (p.total_blocks <= 0) return cudaSuccess;
     const int64_t cap = 16LL * c->num_sms;
     const int grid = (int)(p.total_blocks < cap ? p.total_blocks : cap);
-    k_transfer<<<grid, 256, 0, s>>>(p, c->kpool, c->vpool);
+    k_transfer<<<grid, 256, 0, s>>>(p, reinterpret_cast<uint8_t*>(c->kpool),
+                                    reinterpret_cast<uint8_t*>(c->vpool));
     return cudaGetLastError();
 }
 

@@ -88,12 +88,25 @@ typedef struct sp_config {
     int32_t max_idx_per_seq;   /* RETRIEVAL index capacity per sequence (all its units) */
     int32_t max_tokens;        /* most query rows in one prefill / append call */
     int32_t max_batch;         /* most sequences in one call */
+    int32_t kv_dtype;          /* sp_kv_dtype of the pages (0 = bf16) */
 } sp_config;
+
+/* Element type of the K/V pages.  SP_KV_FP8_E4M3 stores one byte per element
+ * (the KV-cache tutorial's quantisation section: FP8 halves the KV cache,
+ * per-channel scales keep outlier channels from dominating the range): code =
+ * e4m3(x * inv_scale), rounded to nearest even and saturated at +-448, with a
+ * scale per (layer, KV head, dimension) for K and for V set by
+ * sp_set_kv_scales (1.0 until set); the stored value is code * scale.
+ * FP8 pages need head_dim 128.  Decode reads them; prefill of a chunk over
+ * FP8 history pages and sp_rope_realign on FP8 pages return
+ * SP_ERR_UNSUPPORTED. */
+typedef enum { SP_KV_BF16 = 0, SP_KV_FP8_E4M3 = 1 } sp_kv_dtype;
 
 typedef struct sp_cache sp_cache;  /* opaque host handle */
 
 /* Bytes of the three caller-owned device buffers for cfg (host only, no GPU).
- *   pool: K pages then V pages, each [num_pages][page_size][head_dim] bf16.
+ *   pool: K pages then V pages, each [num_pages][page_size][head_dim] elements
+ *         of kv_dtype (bf16, or one byte for FP8).
  *   meta: page tables, policies, retrieval lists, free-page stack, status.
  *   ws:   per-call scratch (prefill work list, decode split partials). */
 sp_status sp_required_bytes(const sp_config* cfg, size_t* pool_bytes,
@@ -189,6 +202,17 @@ sp_status sp_attention_decode_static_scratch(sp_cache* cache, int32_t layer,
                                              const void* q, void* out, float* lse,
                                              void* stream);
 
+/* FP8 pages: the per-channel scales of `layer`.  k_scale, v_scale are host
+ * arrays [num_kv_heads][head_dim] of floats in [2^-14, 128]; the pages store
+ * e4m3(x * (1 / scale)) with the reciprocal taken in fp32.  Decode rebuilds
+ * each element as code * scale in f16 (the scale rounded to f16 first), so the
+ * range keeps scales normal in f16 and 448 * scale below the f16 maximum;
+ * q and P enter the decode MMAs as f16 as well.  Only while no sequence holds
+ * tokens in `layer` (SP_ERR_INVALID_ARG otherwise); for a bf16 cache or a
+ * scale outside the range SP_ERR_INVALID_ARG.  Synchronous. */
+sp_status sp_set_kv_scales(sp_cache* cache, int32_t layer, const float* k_scale,
+                           const float* v_scale, void* stream);
+
 /* RoPE realignment of reused keys (news summary, "Elastic Sparsity": the
  * first recovery step is RoPE position alignment).  For every listed sequence
  * and KV head kv_head (-1 = all KV heads) of `layer`, rotates in place every
@@ -248,7 +272,8 @@ sp_status sp_select_heavy_hitters(const void* q_obs, int32_t n_obs, const void* 
  * (layer count, KV heads, head_dim, page_size, tokens per layer, every unit's
  * policy and retrieval list, per-unit row offsets) followed by the payload:
  * for each (layer, KV head) unit in order, its retained K rows then its
- * retained V rows, [rows][head_dim] bf16 each, in position order (GLOBAL
+ * retained V rows, [rows][head_dim] elements of the page type each (bf16, or
+ * e4m3 bytes for FP8 pages), in position order (GLOBAL
  * every token, LOCAL the sink then the newest ring's worth, RETRIEVAL its
  * listed positions).  *packed_bytes receives the total size; with dst NULL the
  * call only returns that size (no GPU work).  SP_ERR_INVALID_ARG if
@@ -256,8 +281,9 @@ sp_status sp_select_heavy_hitters(const void* q_obs, int32_t n_obs, const void* 
  * `stream`.
  *
  * sp_unpack_seq restores such a buffer into sequence slot `seq` of this cache,
- * which must hold no tokens and have the same layer count, KV heads, head_dim
- * and page_size: it sets the packed policy, allocates pages for every layer
+ * which must hold no tokens and have the same layer count, KV heads, head_dim,
+ * page_size and page type (FP8 scales are the receiver's own: set them equal
+ * before unpacking): it sets the packed policy, allocates pages for every layer
  * and copies the rows into their slots, so the tables, visible sets and
  * attention results equal the source's.  It reads the header (synchronous),
  * checks it against its own size and policies, and checks page capacity
@@ -295,7 +321,7 @@ sp_status sp_free_pages(const sp_cache* cache, int32_t* n);
  *   visible (query, key) pairs of a prefill of rows n0 .. n0+c-1 of (seq, layer),
  *   summed over query heads (FLOP = 4 * head_dim * pairs);
  *   visible K+V bytes one decode query at position t of each listed sequence
- *   reads in `layer`. */
+ *   reads in `layer` (head_dim elements of the page type per row). */
 sp_status sp_count_prefill_pairs(const sp_cache* cache, int32_t seq, int32_t layer,
                                  int64_t n0, int64_t c, int64_t* pairs);
 sp_status sp_count_decode_bytes(const sp_cache* cache, int32_t layer,

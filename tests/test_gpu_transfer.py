@@ -49,9 +49,9 @@ def _bits(t):
 
 
 def _header(buf):
-    h = buf[:88].cpu().numpy().view(np.int64)
+    h = buf[:96].cpu().numpy().view(np.int64)
     return dict(zip(["magic", "version", "layers", "hkv", "head_dim", "page_size", "n_units",
-                     "idx_total", "payload_off", "payload_bytes", "total_bytes"], h.tolist()))
+                     "idx_total", "payload_off", "payload_bytes", "total_bytes", "kv_dtype"], h.tolist()))
 
 
 def test_pack_matches_oracle_bit_exact():
@@ -67,7 +67,8 @@ def test_pack_matches_oracle_bit_exact():
     assert h["magic"] == MAGIC and h["version"] == 1
     assert (h["layers"], h["hkv"], h["head_dim"], h["page_size"], h["n_units"]) == (2, 3, d, P, 6)
     assert h["total_bytes"] == buf.numel() and h["payload_off"] % 256 == 0
-    n_layer = buf[88:88 + 16].cpu().numpy().view(np.int64).tolist()
+    assert h["kv_dtype"] == 0
+    n_layer = buf[96:96 + 16].cpu().numpy().view(np.int64).tolist()
     assert n_layer == [300, 337]
     pt = [[(p.kind, p.sink, p.window, None if p.idx is None else p.idx.tolist()) for p in row]
           for row in pols]
