@@ -319,7 +319,8 @@ sp_status sp_cache_create(const sp_config* cfg, void* pool, void* meta, void* ws
     cudaError_t e = cudaGetDevice(&c->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
     if (e != cudaSuccess) { delete c; return cuda_fail(e, "device query"); }
-    c->decode_ctas = std::min(c->num_sms, kMaxDecodeCtas);
+    // FP8 decode runs two CTAs per SM
+    c->decode_ctas = std::min(c->num_sms * (g.fp8 ? 2 : 1), kMaxDecodeCtas);
     const size_t pool_half = (size_t)cfg->num_pages * cfg->page_size * cfg->head_dim;
     // (FP8 pages: the same pointers address bytes; kernels cast them)
     c->kpool = static_cast<__nv_bfloat16*>(pool);

@@ -32,6 +32,8 @@ namespace {
 constexpr int kConsumerWarps = 4;
 constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxGroup = 16;
+constexpr int kMaxStages = 8;
+constexpr int kItemFirst = 1, kItemLast = 2;   // item flags: first / last of its unit in a CTA
 
 template <int D, int P, bool F8 = false>
 struct DecodeShape {
@@ -40,16 +42,18 @@ struct DecodeShape {
     static constexpr int kHalfBytes = P * 128;
     static constexpr int kTileBytes = kHalves * kHalfBytes;   // K (or V) of one page
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kStageBudget = 160 * 1024;
-    static constexpr int kStages = (kStageBudget / kStageBytes) > 8 ? 8
-                                   : (kStageBudget / kStageBytes) < 2 ? 2
-                                   : (kStageBudget / kStageBytes);
-    static constexpr int kMergeBytes = kConsumerWarps * kMaxGroup * (D + 2) * 4;
-    static constexpr int kSmemBytes = kStages * kStageBytes + kMergeBytes
-                                      + kStages * 16 /*full, empty*/ + kStages * 16 /*desc*/
+    // FP8 runs two CTAs per SM (twice the warps to hide the per-block
+    // latency chain), each with half the stage memory
+    static constexpr int kCtasPerSm = F8 ? 2 : 1;
+    // Shared memory a CTA may use: all of an SM's, or half of it for two CTAs.
+    // The stages get what the merge buffers (sized by the call's group and
+    // grid) and the barriers leave, up to kMaxStages; bf16 stages are capped
+    // at 160 KB (deeper rings measured no faster).
+    static constexpr int kSmemCap = F8 ? 113 * 1024 : 227 * 1024;
+    static constexpr int kStageCap = F8 ? kSmemCap : 160 * 1024;
+    static constexpr int kMiscBytes = kMaxStages * 16 /*full, empty*/ + kMaxStages * 16 /*desc*/
                                       + 16 /*flags*/ + 32 * 16 /*producer batch*/
-                                      + 1024 /*alignment slack*/;
-    static_assert(kSmemBytes <= 227 * 1024, "decode shared memory over the per-CTA limit");
+                                      + 16 /*barrier alignment*/ + 1024 /*base alignment*/;
 };
 
 __device__ __forceinline__ int64_t cta_of_item(int64_t x, int64_t T, int G) {
@@ -57,18 +61,24 @@ __device__ __forceinline__ int64_t cta_of_item(int64_t x, int64_t T, int G) {
 }
 
 template <int D, int P, bool F8>
-__global__ void __launch_bounds__(kDecodeThreads, 1)
+__global__ void __launch_bounds__(kDecodeThreads, F8 ? 2 : 1)
 k_decode(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmK,
          const __grid_constant__ CUtensorMap tmV) {
     using S = DecodeShape<D, P, F8>;
-    constexpr int NST = S::kStages;
+    const int NST = p.nst;
+    constexpr int BK = P >= 32 ? 32 : 16;     // keys per warp block
+    constexpr int NT = BK / 8;                // S n-tiles per block
+    constexpr int NB = P / BK;                // blocks per page (1, 2 or 4)
+    static_assert(NB == 1 || NB == 2 || NB == 4, "blocks per page must divide the warp count");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem;
-    float* merge_o = reinterpret_cast<float*>(smem + NST * S::kStageBytes);  // [4][16][D]
-    float* merge_ml = merge_o + kConsumerWarps * kMaxGroup * D;              // [4][16][2]
-    uint64_t* full = reinterpret_cast<uint64_t*>(merge_ml + kConsumerWarps * kMaxGroup * 2);
+    // merge_o: [4][group][D] partial outputs, later [2][grid][group] merge weights
+    float* merge_o = reinterpret_cast<float*>(smem + NST * S::kStageBytes);
+    float* merge_ml = merge_o + p.merge_floats;                               // [4][group][2]
+    uint64_t* full = reinterpret_cast<uint64_t*>(
+        (reinterpret_cast<uintptr_t>(merge_ml + kConsumerWarps * p.geo.group * 2) + 15) & ~uintptr_t(15));
     uint64_t* empty = full + NST;
     int4* desc = reinterpret_cast<int4*>(empty + NST);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(desc + NST);
@@ -97,7 +107,9 @@ k_decode(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtenso
         // stages and issues the TMA loads in item order.
         if (x0 < x1) {
             if (lane == 0) { prefetch_tmap(&tmK); prefetch_tmap(&tmV); }
-            int64_t issued = 0;
+            int issued = 0;
+            int ps = 0;               // stage of the next load
+            uint32_t pk = 0;          // times that stage has been filled before
             for (int64_t base = x0; base < x1; base += 32) {
                 const int64_t x = base + lane;
                 if (x < x1) {
@@ -130,28 +142,29 @@ k_decode(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtenso
                         atomicOr(p.meta.status, kStatusBadPage);
                         page = 0; lo = hi = 0;          // load something harmless, use nothing
                     }
-                    batch[lane] = make_int4(u, (int)lo, (int)hi, page);
+                    // first / last item of its unit in this CTA's stream
+                    const int fl = ((x == x0 || p.item_off[u] == x) ? kItemFirst : 0) |
+                                   ((x + 1 == x1 || p.item_off[u + 1] == x + 1) ? kItemLast : 0);
+                    batch[lane] = make_int4(u, (int)lo | ((int)hi << 16), page, fl);
                 }
                 __syncwarp();
                 if (lane == 0) {
                     const int n = (int)min64(32, x1 - base);
                     for (int i = 0; i < n; ++i) {
-                        const int64_t xi = base + i;
-                        const int64_t k = (xi - x0) / NST;
-                        const int s = (int)((xi - x0) % NST);
-                        if (k > 0 && !mbar_wait(&empty[s], (uint32_t)((k - 1) & 1), abort_flag, p.meta.status))
+                        if (pk > 0 && !mbar_wait(&empty[ps], (pk - 1) & 1, abort_flag, p.meta.status))
                             break;
                         const int4 bi = batch[i];
-                        desc[s] = make_int4(bi.x, bi.y, bi.z, 0);
-                        mbar_arrive_expect_tx(&full[s], S::kStageBytes);
-                        uint8_t* kdst = stages + s * S::kStageBytes;
+                        desc[ps] = make_int4(bi.x, bi.y, bi.w, 0);
+                        mbar_arrive_expect_tx(&full[ps], S::kStageBytes);
+                        uint8_t* kdst = stages + ps * S::kStageBytes;
                         uint8_t* vdst = kdst + S::kTileBytes;
                         #pragma unroll
                         for (int hh = 0; hh < S::kHalves; ++hh) {
-                            tma_load_2d(kdst + hh * S::kHalfBytes, &tmK, &full[s], hh * 64, bi.w * P);
-                            tma_load_2d(vdst + hh * S::kHalfBytes, &tmV, &full[s], hh * 64, bi.w * P);
+                            tma_load_2d(kdst + hh * S::kHalfBytes, &tmK, &full[ps], hh * 64, bi.z * P);
+                            tma_load_2d(vdst + hh * S::kHalfBytes, &tmV, &full[ps], hh * 64, bi.z * P);
                         }
                         ++issued;
+                        if (++ps == NST) { ps = 0; ++pk; }
                     }
                 }
                 __syncwarp();
@@ -161,7 +174,7 @@ k_decode(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtenso
             // also after an abort).
             if (lane == 0) {
                 for (int s = 0; s < NST && s < issued; ++s) {
-                    const int64_t last_k = (issued - 1 - s) / NST;
+                    const int last_k = (issued - 1 - s) / NST;
                     mbar_wait(&full[s], (uint32_t)(last_k & 1), nullptr, nullptr);
                 }
             }
@@ -187,17 +200,17 @@ k_decode(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtenso
     uint32_t qa[D / 16][4];
     float m_run[2], l_run[2];
     float o_acc[D / 8][4];
-    int cur_u = -1;
+    int b = 0, h = 0;
+    int s = 0;                        // stage of the next item
+    uint32_t ks = 0;                  // times that stage has been filled before
 
-    for (int64_t x = x0; x < x1; ++x) {
-        const int s = (int)((x - x0) % NST);
-        const int64_t k = (x - x0) / NST;
-        if (!mbar_wait(&full[s], (uint32_t)(k & 1), abort_flag, p.meta.status)) break;
+    for (int xi = 0; xi < (int)(x1 - x0); ++xi) {
+        if (!mbar_wait(&full[s], ks & 1, abort_flag, p.meta.status)) break;
         const int4 dd = desc[s];
-        const int u = dd.x, lo = dd.y, hi = dd.z;
-        const int b = u / g.hkv, h = u % g.hkv;
-        if (u != cur_u) {
-            cur_u = u;
+        const int u = dd.x, lo = dd.y & 0xFFFF, hi = dd.y >> 16, fl = dd.z;
+        if (fl & kItemFirst) {
+            b = u / g.hkv;
+            h = u - b * g.hkv;
             const __nv_bfloat16* qb = p.q + ((int64_t)b * g.hq + h * group) * D;
             auto ld = [&](int r, int cc) -> uint32_t {
                 return r < group ? *reinterpret_cast<const uint32_t*>(qb + (int64_t)r * D + cc) : 0u;
@@ -241,141 +254,165 @@ k_decode(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtenso
         }
         const uint32_t kbase = smem_u32(stages + s * S::kStageBytes);
         const uint32_t vbase = kbase + S::kTileBytes;
-        for (int sub = warp; sub < P / 16; sub += kConsumerWarps) {
-            const int key0 = sub * 16;
-            if (key0 >= hi || key0 + 16 <= lo) continue;
-            // S = Q K^T for 16 keys: two n-tiles of 8 keys
-            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        // Blocks of BK keys go to the consumer warps round robin along this
+        // CTA's item stream (block i of item x is block (x - x0) * NB + i),
+        // so every warp has work whatever the page size.
+        const int blk = (warp - ((xi * NB) & 3)) & 3;
+        const int key0 = blk * BK;
+        if (blk < NB && key0 < hi && key0 + BK > lo) {
+            // S = Q K^T for BK keys: NT n-tiles of 8 keys
+            float sc[NT][4];
+            #pragma unroll
+            for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
             if constexpr (F8) {
                 // B fragments straight from the codes: lane (n, j) reads bytes
                 // j*32 .. j*32+31 of key n of each n-tile; word kk of them is
                 // dims j*32 + kk*4 .. +3 (e4m3 -> f16 is exact)
                 const uint8_t* tk = stages + s * S::kStageBytes;
                 const int j = lane & 3, n = lane >> 2;
+                uint32_t w[NT][8];
                 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
+                for (int nt = 0; nt < NT; ++nt) {
                     const int key = key0 + nt * 8 + n;
                     const uint4 c0 = *reinterpret_cast<const uint4*>(tk + sw128(key, 2 * j));
                     const uint4 c1 = *reinterpret_cast<const uint4*>(tk + sw128(key, 2 * j + 1));
-                    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                    w[nt][0] = c0.x; w[nt][1] = c0.y; w[nt][2] = c0.z; w[nt][3] = c0.w;
+                    w[nt][4] = c1.x; w[nt][5] = c1.y; w[nt][6] = c1.z; w[nt][7] = c1.w;
+                }
+                #pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
                     #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
+                    for (int nt = 0; nt < NT; ++nt) {
                         uint32_t b0, b1;
-                        f16x2x2_of_e4m3x4(w[kk], b0, b1);
+                        f16x2x2_of_e4m3x4(w[nt][kk], b0, b1);
                         mma_f16_16816(sc[nt], qa[kk], b0, b1);
                     }
-                }
             } else {
                 const int mi = lane >> 3;
-                const uint32_t key = key0 + (lane & 7) + (mi >= 2 ? 8 : 0);
                 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t chunk = kk * 2 + (mi & 1);
-                    const uint32_t addr = kbase + (chunk >> 3) * S::kHalfBytes + sw128(key, chunk & 7);
-                    uint32_t r0, r1, r2, r3;
-                    ldsm_x4(addr, r0, r1, r2, r3);
-                    mma_bf16_16816(sc[0], qa[kk], r0, r1);
-                    mma_bf16_16816(sc[1], qa[kk], r2, r3);
+                    #pragma unroll
+                    for (int hb = 0; hb < NT / 2; ++hb) {
+                        const uint32_t key = key0 + hb * 16 + (lane & 7) + (mi >= 2 ? 8 : 0);
+                        const uint32_t addr = kbase + (chunk >> 3) * S::kHalfBytes + sw128(key, chunk & 7);
+                        uint32_t r0, r1, r2, r3;
+                        ldsm_x4(addr, r0, r1, r2, r3);
+                        mma_bf16_16816(sc[2 * hb], qa[kk], r0, r1);
+                        mma_bf16_16816(sc[2 * hb + 1], qa[kk], r2, r3);
+                    }
                 }
             }
-            // scale to log2 units, mask keys outside [lo, hi), online softmax
+            // scale to log2 units, mask keys outside [lo, hi) (only for a
+            // block that straddles the range), online softmax
             float mx[2] = {-INFINITY, -INFINITY};
-            #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+            if (key0 >= lo && key0 + BK <= hi) {
                 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int key = key0 + nt * 8 + qc + (e & 1);
-                    float v = sc[nt][e] * p.scale_log2;
-                    if (key < lo || key >= hi) v = -INFINITY;
-                    sc[nt][e] = v;
-                    mx[e >> 1] = fmaxf(mx[e >> 1], v);
-                }
+                for (int nt = 0; nt < NT; ++nt)
+                    #pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        sc[nt][e] *= p.scale_log2;
+                        mx[e >> 1] = fmaxf(mx[e >> 1], sc[nt][e]);
+                    }
+            } else {
+                #pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    #pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int key = key0 + nt * 8 + qc + (e & 1);
+                        float v = sc[nt][e] * p.scale_log2;
+                        if (key < lo || key >= hi) v = -INFINITY;
+                        sc[nt][e] = v;
+                        mx[e >> 1] = fmaxf(mx[e >> 1], v);
+                    }
+            }
             #pragma unroll
             for (int r = 0; r < 2; ++r) {
                 mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
                 mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
             }
-            float alpha[2], mbase[2];
-            #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const float m_new = fmaxf(m_run[r], mx[r]);
-                mbase[r] = m_new == -INFINITY ? 0.f : m_new;
-                alpha[r] = fast_exp2(m_run[r] - mbase[r]);
-                m_run[r] = m_new;
+            // rescale the running state only when a row's maximum grows
+            // (otherwise the factor is exactly 1)
+            if (__any_sync(0xffffffffu, mx[0] > m_run[0] || mx[1] > m_run[1])) {
+                #pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const float m_new = fmaxf(m_run[r], mx[r]);
+                    const float alpha = fast_exp2(m_run[r] - (m_new == -INFINITY ? 0.f : m_new));
+                    m_run[r] = m_new;
+                    l_run[r] *= alpha;
+                    #pragma unroll
+                    for (int nt = 0; nt < D / 8; ++nt) {
+                        o_acc[nt][2 * r] *= alpha;
+                        o_acc[nt][2 * r + 1] *= alpha;
+                    }
+                }
             }
-            float psum[2] = {0.f, 0.f};
+            const float mbase[2] = {m_run[0] == -INFINITY ? 0.f : m_run[0],
+                                    m_run[1] == -INFINITY ? 0.f : m_run[1]};
             #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+            for (int nt = 0; nt < NT; ++nt)
                 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float pv = fast_exp2(sc[nt][e] - mbase[e >> 1]);
                     sc[nt][e] = pv;
-                    psum[e >> 1] += pv;
+                    l_run[e >> 1] += pv;
                 }
+            // O += P V, 16 keys at a time: P from the S fragments (rows = heads)
             #pragma unroll
-            for (int r = 0; r < 2; ++r) l_run[r] = l_run[r] * alpha[r] + psum[r];
-            #pragma unroll
-            for (int nt = 0; nt < D / 8; ++nt) {
-                o_acc[nt][0] *= alpha[0]; o_acc[nt][1] *= alpha[0];
-                o_acc[nt][2] *= alpha[1]; o_acc[nt][3] *= alpha[1];
-            }
-            // O += P V: P from the S fragments (rows = heads, k = keys)
-            uint32_t pa[4];
-            if constexpr (F8) {
-                pa[0] = pack_f16(sc[0][0], sc[0][1]);
-                pa[1] = pack_f16(sc[0][2], sc[0][3]);
-                pa[2] = pack_f16(sc[1][0], sc[1][1]);
-                pa[3] = pack_f16(sc[1][2], sc[1][3]);
-            } else {
-                pa[0] = pack_bf16(sc[0][0], sc[0][1]);
-                pa[1] = pack_bf16(sc[0][2], sc[0][3]);
-                pa[2] = pack_bf16(sc[1][0], sc[1][1]);
-                pa[3] = pack_bf16(sc[1][2], sc[1][3]);
-            }
-            if constexpr (F8) {
-                // The output dims of n-tile nt, column n are n*16 + nt, so lane
-                // (n, j) needs dims n*16 .. n*16+15 (chunk n) of keys 2j, 2j+1,
-                // 2j+8, 2j+9; byte interleaves pair consecutive keys per dim.
-                // V's scales are applied to the finished sums.
-                const uint8_t* tv = stages + s * S::kStageBytes + S::kTileBytes;
-                const int j = lane & 3, n = lane >> 2;
-                const uint4 r0 = *reinterpret_cast<const uint4*>(tv + sw128(key0 + 2 * j, n));
-                const uint4 r1 = *reinterpret_cast<const uint4*>(tv + sw128(key0 + 2 * j + 1, n));
-                const uint4 r8 = *reinterpret_cast<const uint4*>(tv + sw128(key0 + 2 * j + 8, n));
-                const uint4 r9 = *reinterpret_cast<const uint4*>(tv + sw128(key0 + 2 * j + 9, n));
-                const uint32_t a0[4] = {r0.x, r0.y, r0.z, r0.w}, a1[4] = {r1.x, r1.y, r1.z, r1.w};
-                const uint32_t a8[4] = {r8.x, r8.y, r8.z, r8.w}, a9[4] = {r9.x, r9.y, r9.z, r9.w};
-                #pragma unroll
-                for (int w = 0; w < 4; ++w) {            // dims n*16 + 4w .. +3: n-tiles 4w .. 4w+3
-                    uint32_t lo0, lo1, lo2, lo3, hi0, hi1, hi2, hi3;
-                    f16x2x2_of_e4m3x4(prmt(a0[w], a1[w], 0x5140u), lo0, lo1);   // bytes 0,1
-                    f16x2x2_of_e4m3x4(prmt(a0[w], a1[w], 0x7362u), lo2, lo3);   // bytes 2,3
-                    f16x2x2_of_e4m3x4(prmt(a8[w], a9[w], 0x5140u), hi0, hi1);
-                    f16x2x2_of_e4m3x4(prmt(a8[w], a9[w], 0x7362u), hi2, hi3);
-                    mma_f16_16816(o_acc[4 * w + 0], pa, lo0, hi0);
-                    mma_f16_16816(o_acc[4 * w + 1], pa, lo1, hi1);
-                    mma_f16_16816(o_acc[4 * w + 2], pa, lo2, hi2);
-                    mma_f16_16816(o_acc[4 * w + 3], pa, lo3, hi3);
-                }
-            } else {
-                const int mi = lane >> 3;
-                const uint32_t key = key0 + (lane & 7) + ((mi & 1) ? 8 : 0);
-                #pragma unroll
-                for (int np = 0; np < D / 16; ++np) {
-                    const uint32_t chunk = np * 2 + (mi >> 1);
-                    const uint32_t addr = vbase + (chunk >> 3) * S::kHalfBytes + sw128(key, chunk & 7);
-                    uint32_t r0, r1, r2, r3;
-                    ldsm_x4_t(addr, r0, r1, r2, r3);
-                    mma_bf16_16816(o_acc[2 * np], pa, r0, r1);
-                    mma_bf16_16816(o_acc[2 * np + 1], pa, r2, r3);
+            for (int hb = 0; hb < NT / 2; ++hb) {
+                uint32_t pa[4];
+                if constexpr (F8) {
+                    pa[0] = pack_f16(sc[2 * hb][0], sc[2 * hb][1]);
+                    pa[1] = pack_f16(sc[2 * hb][2], sc[2 * hb][3]);
+                    pa[2] = pack_f16(sc[2 * hb + 1][0], sc[2 * hb + 1][1]);
+                    pa[3] = pack_f16(sc[2 * hb + 1][2], sc[2 * hb + 1][3]);
+                    // The output dims of n-tile nt, column n are n*16 + nt, so
+                    // lane (n, j) needs dims n*16 .. n*16+15 (chunk n) of keys
+                    // 2j, 2j+1, 2j+8, 2j+9; byte interleaves pair consecutive
+                    // keys per dim.  V's scales are applied to the finished sums.
+                    const uint8_t* tv = stages + s * S::kStageBytes + S::kTileBytes;
+                    const int j = lane & 3, n = lane >> 2, kb = key0 + hb * 16 + 2 * j;
+                    const uint4 r0 = *reinterpret_cast<const uint4*>(tv + sw128(kb, n));
+                    const uint4 r1 = *reinterpret_cast<const uint4*>(tv + sw128(kb + 1, n));
+                    const uint4 r8 = *reinterpret_cast<const uint4*>(tv + sw128(kb + 8, n));
+                    const uint4 r9 = *reinterpret_cast<const uint4*>(tv + sw128(kb + 9, n));
+                    const uint32_t a0[4] = {r0.x, r0.y, r0.z, r0.w}, a1[4] = {r1.x, r1.y, r1.z, r1.w};
+                    const uint32_t a8[4] = {r8.x, r8.y, r8.z, r8.w}, a9[4] = {r9.x, r9.y, r9.z, r9.w};
+                    #pragma unroll
+                    for (int wd = 0; wd < 4; ++wd) {     // dims n*16 + 4wd .. +3: n-tiles 4wd .. 4wd+3
+                        uint32_t lo0, lo1, lo2, lo3, hi0, hi1, hi2, hi3;
+                        f16x2x2_of_e4m3x4(prmt(a0[wd], a1[wd], 0x5140u), lo0, lo1);   // bytes 0,1
+                        f16x2x2_of_e4m3x4(prmt(a0[wd], a1[wd], 0x7362u), lo2, lo3);   // bytes 2,3
+                        f16x2x2_of_e4m3x4(prmt(a8[wd], a9[wd], 0x5140u), hi0, hi1);
+                        f16x2x2_of_e4m3x4(prmt(a8[wd], a9[wd], 0x7362u), hi2, hi3);
+                        mma_f16_16816(o_acc[4 * wd + 0], pa, lo0, hi0);
+                        mma_f16_16816(o_acc[4 * wd + 1], pa, lo1, hi1);
+                        mma_f16_16816(o_acc[4 * wd + 2], pa, lo2, hi2);
+                        mma_f16_16816(o_acc[4 * wd + 3], pa, lo3, hi3);
+                    }
+                } else {
+                    pa[0] = pack_bf16(sc[2 * hb][0], sc[2 * hb][1]);
+                    pa[1] = pack_bf16(sc[2 * hb][2], sc[2 * hb][3]);
+                    pa[2] = pack_bf16(sc[2 * hb + 1][0], sc[2 * hb + 1][1]);
+                    pa[3] = pack_bf16(sc[2 * hb + 1][2], sc[2 * hb + 1][3]);
+                    const int mi = lane >> 3;
+                    const uint32_t key = key0 + hb * 16 + (lane & 7) + ((mi & 1) ? 8 : 0);
+                    #pragma unroll
+                    for (int np = 0; np < D / 16; ++np) {
+                        const uint32_t chunk = np * 2 + (mi >> 1);
+                        const uint32_t addr = vbase + (chunk >> 3) * S::kHalfBytes + sw128(key, chunk & 7);
+                        uint32_t r0, r1, r2, r3;
+                        ldsm_x4_t(addr, r0, r1, r2, r3);
+                        mma_bf16_16816(o_acc[2 * np], pa, r0, r1);
+                        mma_bf16_16816(o_acc[2 * np + 1], pa, r2, r3);
+                    }
                 }
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
-
-        const bool unit_ends = (x + 1 == x1) || (p.item_off[u + 1] == x + 1);
-        if (!unit_ends) continue;
+        if (++s == NST) { s = 0; ++ks; }
+        if (!(fl & kItemLast)) continue;
 
         // ------------- merge the four warps' partial states -------------
         #pragma unroll
@@ -387,7 +424,7 @@ k_decode(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtenso
         for (int r = 0; r < 2; ++r) {
             const int row = qr + 8 * r;
             if (row < group) {
-                float* mo = merge_o + ((size_t)warp * kMaxGroup + row) * D;
+                float* mo = merge_o + ((size_t)warp * group + row) * D;
                 if constexpr (F8) {       // column c of n-tile nt is dim c*16 + nt; times V's scale
                     const float* vs = p.meta.vscale + ((int64_t)p.layer * g.hkv + h) * D;
                     #pragma unroll
@@ -404,8 +441,8 @@ k_decode(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtenso
                     }
                 }
                 if ((lane & 3) == 0) {
-                    merge_ml[(warp * kMaxGroup + row) * 2] = m_run[r];
-                    merge_ml[(warp * kMaxGroup + row) * 2 + 1] = l_run[r];
+                    merge_ml[(warp * group + row) * 2] = m_run[r];
+                    merge_ml[(warp * group + row) * 2 + 1] = l_run[r];
                 }
             }
         }
@@ -419,13 +456,13 @@ k_decode(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtenso
             const int r = e / D, col = e % D;
             float mst = -INFINITY;
             #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) mst = fmaxf(mst, merge_ml[(w * kMaxGroup + r) * 2]);
+            for (int w = 0; w < kConsumerWarps; ++w) mst = fmaxf(mst, merge_ml[(w * group + r) * 2]);
             float lst = 0.f, ost = 0.f;
             #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) {
-                const float sc_w = fast_exp2(merge_ml[(w * kMaxGroup + r) * 2] - mst);
-                lst += sc_w * merge_ml[(w * kMaxGroup + r) * 2 + 1];
-                ost += sc_w * merge_o[((size_t)w * kMaxGroup + r) * D + col];
+                const float sc_w = fast_exp2(merge_ml[(w * group + r) * 2] - mst);
+                lst += sc_w * merge_ml[(w * group + r) * 2 + 1];
+                ost += sc_w * merge_o[((size_t)w * group + r) * D + col];
             }
             const int64_t orow = (int64_t)b * g.hq + h * group + r;
             if (whole) {
@@ -459,7 +496,7 @@ k_decode(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtenso
                 __threadfence();
                 const int nseg = c_last - c_first + 1;
                 float* wts = merge_o;                          // [nseg][group] weights
-                float* mls = merge_o + kConsumerWarps * kMaxGroup * D / 2;  // [nseg][group] l
+                float* mls = merge_o + p.merge_floats / 2;     // [nseg][group] l
                 float* mstar = merge_ml;                       // [group] m*, then 1 / l*
                 for (int e = ctid; e < nseg * group; e += kConsumerWarps * 32) {
                     const int sg = e / group, r = e % group;
@@ -518,18 +555,33 @@ k_decode(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtenso
 }
 
 template <int D, int P, bool F8 = false>
-cudaError_t launch_decode_t(const sp_cache* c, const DecodeParams& p, int grid, cudaStream_t s) {
+cudaError_t launch_decode_t(const sp_cache* c, DecodeParams& p, int grid, cudaStream_t s) {
     using Sh = DecodeShape<D, P, F8>;
+    // merge buffer: the four warps' [group][D] partials, or two [grid][group]
+    // arrays for the cross-CTA merge, whichever is larger (a multiple of 4)
+    const int group = c->geo.group;
+    const int mo = std::max(kConsumerWarps * group * D, 2 * grid * group);
+    p.merge_floats = (mo + 3) & ~3;
+    const int merge_bytes = (p.merge_floats + kConsumerWarps * group * 2) * 4;
+    const int room = std::min(Sh::kStageCap, Sh::kSmemCap - merge_bytes - Sh::kMiscBytes);
+    p.nst = std::min(kMaxStages, room / Sh::kStageBytes);
+    if (p.nst < 2) return cudaErrorInvalidConfiguration;
+    const int smem = p.nst * Sh::kStageBytes + merge_bytes + Sh::kMiscBytes;
     cudaError_t e = cudaFuncSetAttribute(k_decode<D, P, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Sh::kSmemBytes);
+                                         Sh::kSmemCap);
     if (e != cudaSuccess) return e;
-    k_decode<D, P, F8><<<grid, kDecodeThreads, Sh::kSmemBytes, s>>>(p, c->tm_kpool, c->tm_vpool);
+    if (Sh::kCtasPerSm > 1) {
+        e = cudaFuncSetAttribute(k_decode<D, P, F8>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+    }
+    k_decode<D, P, F8><<<grid, kDecodeThreads, smem, s>>>(p, c->tm_kpool, c->tm_vpool);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_decode(const sp_cache* c, const DecodeParams& p, cudaStream_t s) {
+cudaError_t launch_decode(const sp_cache* c, DecodeParams& p, cudaStream_t s) {
     // Persistent grid, but at least kMinItemsPerCta pages per CTA: a small batch
     // then spreads one head over a few CTAs instead of dozens (fewer partials
     // to merge).
@@ -537,9 +589,6 @@ cudaError_t launch_decode(const sp_cache* c, const DecodeParams& p, cudaStream_t
     int grid = c->decode_ctas;
     const int64_t want = (p.total_items + kMinItemsPerCta - 1) / kMinItemsPerCta;
     if (want < grid) grid = (int)(want > 0 ? want : 1);
-    // the merge stages up to grid x group (m, l) pairs in half of the merge buffer
-    const int merge_cap = kConsumerWarps * kMaxGroup * c->geo.d / 2 / c->geo.group;
-    if (grid > merge_cap) grid = merge_cap;
     const int D = c->geo.d, P = c->geo.page;
     if (c->geo.fp8) {   // FP8 pages: head_dim 128 only (checked at create)
         if (D != 128) return cudaErrorInvalidValue;

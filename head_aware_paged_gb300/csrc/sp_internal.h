@@ -69,6 +69,8 @@ struct DecodeParams {
     float* part_ml;              // [(n_units + grid)][group][2]
     int32_t* counters;           // [n_units], zero between calls
     float scale_log2;            // log2(e) / sqrt(d)
+    int32_t nst;                 // pipeline stages (set by the launcher)
+    int32_t merge_floats;        // merge buffer floats (set by the launcher)
 };
 
 // RoPE realignment of stored K rows (sp_rope.cu), one launch per call.
@@ -185,7 +187,7 @@ cudaError_t launch_export(const sp_cache* c, int seq, int layer, int h, int32_t*
                           int32_t* out_pos, cudaStream_t s);
 cudaError_t launch_decode_counts(const sp_cache* c, int seq, int layer, int h,
                                  const int64_t* pos, int n, int32_t* out, cudaStream_t s);
-cudaError_t launch_decode(const sp_cache* c, const DecodeParams& p, cudaStream_t s);
+cudaError_t launch_decode(const sp_cache* c, DecodeParams& p, cudaStream_t s);
 cudaError_t launch_rope(const sp_cache* c, const RopeParams& p, cudaStream_t s);
 cudaError_t launch_transfer(const sp_cache* c, const TransferParams& p, cudaStream_t s);
 
