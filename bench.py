@@ -365,7 +365,8 @@ def run_ours(args, ws, rank):
     wl = W.WORKLOADS[args.workload]
     decode = wl.decode_steps > 0 and wl.name.startswith("llama3_8b")
     if args.kv_dtype == "fp8" and not decode:
-        raise SystemExit("--kv-dtype fp8 applies to the decode workload (prefill over FP8 history is not built)")
+        raise SystemExit("--kv-dtype fp8 applies to the decode workload and --op chunk_prefill "
+                         "(the prefill step has no cached history)")
     if decode:
         st = DecodeStep(wl, layers=args.decode_layers or None, fp8=args.kv_dtype == "fp8")
     else:
@@ -668,6 +669,71 @@ def run_op_rope(args):
             "clocks": clk}
 
 
+def run_op_chunk(args):
+    """Chunked prefill over cached history: the Mistral-7B-shaped layer's
+    policies, 8,192 tokens already in the cache (bf16 or FP8 pages), then a
+    2,048-row chunk prefilled over them (CUDA events around the call; the
+    chunk is re-run on the same history each step)."""
+    import torch
+    from head_aware_paged_gb300 import KV_BF16, KV_FP8, Config, Policy, SegPagedCache
+    wl = W.WORKLOADS["mistral7b_prefill_8k"]
+    fp8 = args.kv_dtype == "fp8"
+    layer = bench_layer(wl)
+    row = W.policies(wl)[layer]
+    H, C = 8192, 2048
+    pol = [[Policy(p.kind, p.sink, p.window, None if p.idx is None else p.idx.tolist()) for p in row]]
+    pages = len(row) * ((H + C) // wl.page + 4)
+    cache = SegPagedCache(Config(num_layers=1, num_q_heads=wl.hq, num_kv_heads=wl.hkv, head_dim=wl.d,
+                                 page_size=wl.page, max_seqs=1, max_seq_len=H + C + 64, num_pages=pages,
+                                 max_idx_per_seq=max(1, sum(0 if p.idx is None else len(p.idx) for p in row)),
+                                 max_tokens=H + C, max_batch=1, kv_dtype=KV_FP8 if fp8 else KV_BF16))
+    cache.set_policy(0, pol)
+    q, k, v = W.qkv(wl, H + C, 0, 0, device="cuda")
+    if fp8:
+        sc = np.full((wl.hkv, wl.d), FP8_SCALE, np.float32)
+        cache.set_kv_scales(0, sc, sc)
+    cache.build(0, 0, k[:H].contiguous(), v[:H].contiguous())
+    qc, kc, vc = q[H:].contiguous(), k[H:].contiguous(), v[H:].contiguous()
+    out = torch.empty_like(qc)
+    lse = torch.empty(C, wl.hq, dtype=torch.float32, device="cuda")
+    flop = 4 * wl.d * cache.count_prefill_pairs(0, 0, H, C)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup):
+        cache.prefill(0, [0], [0, C], qc, kc, vc, out, lse)
+    torch.cuda.synchronize()
+    peaks, src = load_peaks()
+    props = torch.cuda.get_device_properties(0)
+    u = str(getattr(props, "uuid", ""))
+    clocks = ClockSampler(u if u.startswith("GPU-") else ("GPU-" + u if u else None))
+    clocks.start()
+    time.sleep(0.4)
+    ms = []
+    for _ in range(args.steps):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        cache.prefill(0, [0], [0, C], qc, kc, vc, out, lse)
+        b.record()
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    clk = clocks.stop()
+    assert cache.status() == 0
+    total = sum(ms)
+    tf = flop * args.steps / (total / 1e3) / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    return {"metric": "chunked prefill over cached history, TFLOP/s over visible pairs",
+            "op": "chunk_prefill", "value": tf, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total / args.steps, "higher_is_better": True,
+            "dtype": "bf16 MMA; history pages " + ("e4m3 (converted to bf16 in shared memory)" if fp8 else "bf16"),
+            "data": "synthetic (seeded N(0,1), pages' shapes)",
+            "config": {"workload": "mistral7b layer %d policies, %d cached tokens + %d-row chunk" % (layer, H, C),
+                       "kv_dtype": "fp8_e4m3" if fp8 else "bf16", "flop_per_call": flop,
+                       "l2": "flushed between calls"},
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tf / peak, "kernel": "k_prefill", "peak_source": src + " bf16_tflops (burst)"},
+            "clocks": clk}
+
+
 def run_op_pack(args):
     """sp_pack_seq of Llama-3-8B-shaped sequences (32 layers x 8 KV heads x
     32,768 tokens, the decode workload's policies): HBM-bound, every retained
@@ -788,13 +854,14 @@ def main():
                     help="decode workload: run only the first N layers (profiling a small case)")
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
                     help="decode workload: page element type (fp8 = e4m3 codes with per-channel scales)")
-    ap.add_argument("--op", default="", choices=["", "rope_realign", "pack", "select"],
+    ap.add_argument("--op", default="", choices=["", "rope_realign", "pack", "select", "chunk_prefill"],
                     help="time one library operation instead of the attention step")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.op:
-        line = {"rope_realign": run_op_rope, "pack": run_op_pack, "select": run_op_select}[args.op](args)
+        line = {"rope_realign": run_op_rope, "pack": run_op_pack, "select": run_op_select,
+                "chunk_prefill": run_op_chunk}[args.op](args)
         print(json.dumps(line), flush=True)
         return
     if args.impl == "reference":

@@ -540,11 +540,6 @@ sp_status sp_attention_prefill(sp_cache* c, int32_t layer, const int32_t* seq_id
             return fail(SP_ERR_INVALID_ARG, "chunk would pass max_seq_len");
     }
     if (cu_q[n_seqs] > c->cfg.max_tokens) return fail(SP_ERR_INVALID_ARG, "more rows than max_tokens");
-    if (c->geo.fp8)
-        for (int b = 0; b < n_seqs; ++b)
-            if (c->h_seqlen[(size_t)seq_ids[b] * c->cfg.num_layers + layer] != 0)
-                return fail(SP_ERR_UNSUPPORTED, "prefill over FP8 history pages is not built "
-                                                "(a chunk with no history is)");
     return prefill_impl(c, layer, seq_ids, n_seqs, cu_q, static_cast<const __nv_bfloat16*>(q),
                         static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v),
                         static_cast<__nv_bfloat16*>(out), lse, static_cast<cudaStream_t>(stream));

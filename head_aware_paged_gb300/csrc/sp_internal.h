@@ -156,7 +156,7 @@ struct sp_cache {
     cudaEvent_t stage_ev[kStaging] = {};
     size_t stage_bytes = 0;                       // size of each buffer
     int stage_next = 0;
-    bool prefill_checked[2][4] = {};             // [D == 128][log2(P) - 4]: attributes set
+    bool prefill_checked[3][4] = {};             // [FP8 ? 2 : D == 128][log2(P) - 4]: attributes set
     ~sp_cache();
 };
 

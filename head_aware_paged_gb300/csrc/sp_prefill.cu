@@ -80,13 +80,16 @@ struct PrefillParams {
     int32_t row0[kMaxCallSeqs];  // first chunk row in q / k / v
 };
 
-template <int D>
+template <int D, bool F8 = false>
 struct PfShape {
     static constexpr int kHalves = D / 64;
     static constexpr int kHalfBytes = 128 * 128;            // 128 rows x 128 bytes
     static constexpr int kQBytes = kHalves * kHalfBytes;     // one Q tile
     static constexpr int kKVBytes = kHalves * kHalfBytes;    // one K or V tile
-    static constexpr int kFixed = 2 * kQBytes;
+    // FP8 history pages land in one of two code slots (128 keys x 128 bytes)
+    // before the converter warps write them into a bf16 stage
+    static constexpr int kF8Slot = 128 * 128;
+    static constexpr int kFixed = 2 * kQBytes + (F8 ? 2 * kF8Slot : 0);
     static constexpr int kMisc = 2048;                       // barriers, flags, alignment slack
     static constexpr int kStagesFit = (kSmemLimit - kFixed - kMisc) / kKVBytes;
     static constexpr int kStages = kStagesFit > 6 ? 6 : kStagesFit;
@@ -163,19 +166,20 @@ __device__ __forceinline__ uint32_t lowmask32(int32_t n) {
     return n <= 0 ? 0u : n >= 32 ? 0xFFFFFFFFu : ((1u << n) - 1u);
 }
 
-template <int D, int P>
+template <int D, int P, bool F8>
 __global__ void __launch_bounds__(kPfThreads, 1)
 k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tmQ,
           const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
           const __grid_constant__ CUtensorMap tmKp, const __grid_constant__ CUtensorMap tmVp) {
-    using S = PfShape<D>;
+    using S = PfShape<D, F8>;
     constexpr int NS = S::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = smem;                               // [2][halves][128][128 B]
     uint8_t* sKV = sQ + 2 * S::kQBytes;               // [NS][halves][128][128 B]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + NS * S::kKVBytes);
+    uint8_t* sF8 = sKV + NS * S::kKVBytes;            // FP8 only: [2][128][128 B] code slots
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sF8 + (F8 ? 2 * S::kF8Slot : 0));
     uint64_t* q_full = bars;
     uint64_t* q_empty = bars + 1;
     uint64_t* kv_full = bars + 2;
@@ -185,12 +189,19 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
     uint64_t* o_full = p_full + 2;                    // [2]
     uint64_t* o_empty = o_full + 2;                   // [2]
     uint64_t* mma_done = o_empty + 2;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mma_done + 1);
+    uint64_t* f_full = mma_done + 1;                  // [2] FP8 code slot landed
+    uint64_t* f_empty = f_full + 2;                   // [2] FP8 code slot converted
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(f_empty + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     // MMA width (keys) of the tile each K/V stage holds, written by the
     // producer before the stage's copies; read by the MMA thread after the
     // stage's full barrier (the arrive orders the write before it)
     volatile int32_t* stage_keys = abort_flag + 4;
+    // FP8: the conversion job of each code slot {bf16 stage, K or V, KV head,
+    // rows}, or {-1, ...} = no more jobs; written by the producer before the
+    // slot's full barrier
+    int4* jobs = reinterpret_cast<int4*>(
+        (reinterpret_cast<uintptr_t>(stage_keys + 8) + 15) & ~uintptr_t(15));
     int* status = p.meta.status;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -209,6 +220,7 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
             mbar_init(&o_empty[t], 4);
         }
         mbar_init(mma_done, 1);
+        for (int f = 0; f < 2; ++f) { mbar_init(&f_full[f], 1); mbar_init(&f_empty[f], 1); }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -227,7 +239,7 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
         // ------------------------------ producer ------------------------------
         prefetch_tmap(&tmQ); prefetch_tmap(&tmK); prefetch_tmap(&tmV);
         prefetch_tmap(&tmKp); prefetch_tmap(&tmVp);
-        uint32_t q_loads = 0, L = 0;
+        uint32_t q_loads = 0, L = 0, F = 0;     // F: FP8 code slots filled
         bool ok = true;
         for (int n = p.cta_off[cta]; n < p.cta_off[cta + 1] && ok; ++n) {
             const Item it = load_item(p, n);
@@ -261,7 +273,7 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                     for (int pg = 0; pg < np; ++pg) {
                         const int32_t phys = it.ptab[pk.start / P + pg];
                         if (phys < 0 || phys >= g.num_pages) continue;
-                        for (int hf = 0; hf < S::kHalves; ++hf) {
+                        for (int hf = 0; hf < (F8 ? 1 : S::kHalves); ++hf) {   // FP8 rows: one 128-byte box
                             tma_prefetch_2d(&tmKp, hf * 64, phys * P);
                             tma_prefetch_2d(&tmVp, hf * 64, phys * P);
                         }
@@ -294,6 +306,21 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                         for (int hf = 0; hf < S::kHalves; ++hf)
                             tma_load_2d(dst + hf * S::kHalfBytes, kv ? &tmV : &tmK, &kv_full[st],
                                         it.kvh * D + hf * 64, y);
+                    } else if (F8) {
+                        // codes into the next slot; a converter warp turns them into
+                        // bf16 rows of stage st and completes kv_full[st] itself
+                        const int np = (kt.nkeys + P - 1) / P;
+                        const uint32_t f = F & 1, fr = F >> 1;
+                        if (fr > 0 && !mbar_wait(&f_empty[f], (fr - 1) & 1, abort_flag, status)) { ok = false; break; }
+                        jobs[f] = make_int4((int)st, kv, it.kvh, np * P);
+                        mbar_arrive_expect_tx(&f_full[f], np * P * 128);
+                        for (int pg = 0; pg < np; ++pg) {
+                            int32_t phys = it.ptab[kt.start / P + pg];
+                            if (phys < 0 || phys >= g.num_pages) { atomicOr(status, kStatusBadPage); phys = 0; }
+                            tma_load_2d(sF8 + f * S::kF8Slot + pg * P * 128, kv ? &tmVp : &tmKp,
+                                        &f_full[f], 0, phys * P);
+                        }
+                        ++F;
                     } else {
                         const int np = (kt.nkeys + P - 1) / P;
                         mbar_arrive_expect_tx(&kv_full[st], np * P * 128 * S::kHalves);
@@ -309,7 +336,16 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                 }
             }
         }
-        // drain: every copy issued has landed before the CTA may exit
+        if (F8) {
+            // no more conversion jobs: an empty job through the next slot
+            const uint32_t f = F & 1, fr = F >> 1;
+            if (fr == 0 || mbar_wait(&f_empty[f], (fr - 1) & 1, abort_flag, status)) {
+                jobs[f] = make_int4(-1, 0, 0, 0);
+                mbar_arrive(&f_full[f]);
+            }
+        }
+        // drain: every copy issued has landed before the CTA may exit (FP8
+        // stages complete when converted, after their codes landed)
         for (uint32_t s = 0; s < NS && s < L; ++s)
             mbar_wait(&kv_full[s], ((L - 1 - s) / NS) & 1, nullptr, nullptr);
         if (q_loads > 0) mbar_wait(q_full, (q_loads - 1) & 1, nullptr, nullptr);
@@ -432,6 +468,51 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
         // all MMAs issued by this thread complete before TMEM can be freed
         tc_commit(mma_done);
         mbar_wait(mma_done, 0, nullptr, nullptr);
+      } else if (F8 && warp >= 10) {
+        // ------------------ FP8 history: codes -> bf16 stage rows ------------------
+        // 64 threads: thread (row r0 of each 8, 16-code chunk c16) writes
+        // bf16(code * scale) of dims c16*16 .. +15 into the 128-byte-swizzled
+        // K-major layout the MMA reads (two 64-dim halves per row).
+        const int ct = threadIdx.x - 320;
+        const int c16 = ct & 7, r0 = ct >> 3;
+        uint32_t fj = 0;
+        while (true) {
+            const uint32_t f = fj & 1;
+            if (!mbar_wait(&f_full[f], (fj >> 1) & 1, abort_flag, status)) break;
+            const int4 jb = jobs[f];
+            if (jb.x < 0) break;
+            const float* scp = (jb.y ? p.meta.vscale : p.meta.kscale) +
+                               ((int64_t)p.layer * g.hkv + jb.z) * D + c16 * 16;
+            float sc[16];
+            #pragma unroll
+            for (int e = 0; e < 16; e += 4) {
+                const float4 v4 = __ldg(reinterpret_cast<const float4*>(scp + e));
+                sc[e] = v4.x; sc[e + 1] = v4.y; sc[e + 2] = v4.z; sc[e + 3] = v4.w;
+            }
+            const uint8_t* src = sF8 + f * S::kF8Slot;
+            uint8_t* dst = sKV + jb.x * S::kKVBytes + (c16 >> 2) * S::kHalfBytes;
+            const uint32_t ch = (c16 & 3) * 2;
+            for (int r = r0; r < jb.w; r += 8) {
+                const uint4 q4 = *reinterpret_cast<const uint4*>(src + sw128(r, c16));
+                const uint32_t w[4] = {q4.x, q4.y, q4.z, q4.w};
+                uint32_t o[8];
+                #pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint32_t h2 = f16x2_of_e4m3x2((w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);
+                    const __half2 hv = *reinterpret_cast<const __half2*>(&h2);
+                    o[e] = pack_bf16(__low2float(hv) * sc[2 * e], __high2float(hv) * sc[2 * e + 1]);
+                }
+                *reinterpret_cast<uint4*>(dst + sw128(r, ch)) = make_uint4(o[0], o[1], o[2], o[3]);
+                *reinterpret_cast<uint4*>(dst + sw128(r, ch + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+            }
+            fence_async_smem();                       // rows visible to the tensor core
+            asm volatile("bar.sync 2, 64;" ::: "memory");
+            if (ct == 0) {
+                mbar_arrive(&f_empty[f]);
+                mbar_arrive(&kv_full[jb.x]);
+            }
+            ++fj;
+        }
       }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kHighRegs));
@@ -668,24 +749,24 @@ __global__ void k_prefill_counts(Meta meta, Geo g, int seq, int layer, int h,
     }
 }
 
-template <int D, int P>
+template <int D, int P, bool F8 = false>
 cudaError_t launch_prefill_t(sp_cache* c, const PrefillParams& p, int grid,
                              const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                              cudaStream_t s) {
-    using Sh = PfShape<D>;
-    bool& checked = c->prefill_checked[D == 128][P == 16 ? 0 : P == 32 ? 1 : P == 64 ? 2 : 3];
+    using Sh = PfShape<D, F8>;
+    bool& checked = c->prefill_checked[F8 ? 2 : D == 128][P == 16 ? 0 : P == 32 ? 1 : P == 64 ? 2 : 3];
     if (!checked) {   // once per cache and kernel instance
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, k_prefill<D, P>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, k_prefill<D, P, F8>);
         if (e != cudaSuccess) return e;
         // The setmaxnreg split assumes exactly kLaunchRegs registers per thread
         // at launch; anything else could leave an increase waiting forever.
         if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(k_prefill<D, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmem);
+        e = cudaFuncSetAttribute(k_prefill<D, P, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmem);
         if (e != cudaSuccess) return e;
         checked = true;
     }
-    k_prefill<D, P><<<grid, kPfThreads, Sh::kSmem, s>>>(p, tq, tk, tv, c->tm_kpool, c->tm_vpool);
+    k_prefill<D, P, F8><<<grid, kPfThreads, Sh::kSmem, s>>>(p, tq, tk, tv, c->tm_kpool, c->tm_vpool);
     return cudaGetLastError();
 }
 
@@ -791,10 +872,18 @@ sp_status prefill_impl(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32
         return fail(SP_ERR_CUDA, err);
 #define SP_PF(DD, PP) \
     if (D == DD && P == PP) e = launch_prefill_t<DD, PP>(c, p, grid, tq, tk, tv, stream); else
-    SP_PF(64, 16) SP_PF(64, 32) SP_PF(64, 64) SP_PF(64, 128)
-    SP_PF(128, 16) SP_PF(128, 32) SP_PF(128, 64) SP_PF(128, 128)
-    e = cudaErrorInvalidValue;
+#define SP_PF8(PP) \
+    if (D == 128 && P == PP) e = launch_prefill_t<128, PP, true>(c, p, grid, tq, tk, tv, stream); else
+    if (c->geo.fp8) {   // FP8 pages (head_dim 128, checked at create)
+        SP_PF8(16) SP_PF8(32) SP_PF8(64) SP_PF8(128)
+        e = cudaErrorInvalidValue;
+    } else {
+        SP_PF(64, 16) SP_PF(64, 32) SP_PF(64, 64) SP_PF(64, 128)
+        SP_PF(128, 16) SP_PF(128, 32) SP_PF(128, 64) SP_PF(128, 128)
+        e = cudaErrorInvalidValue;
+    }
 #undef SP_PF
+#undef SP_PF8
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     return SP_OK;
 }

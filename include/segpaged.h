@@ -97,9 +97,11 @@ typedef struct sp_config {
  * e4m3(x * inv_scale), rounded to nearest even and saturated at +-448, with a
  * scale per (layer, KV head, dimension) for K and for V set by
  * sp_set_kv_scales (1.0 until set); the stored value is code * scale.
- * FP8 pages need head_dim 128.  Decode reads them; prefill of a chunk over
- * FP8 history pages and sp_rope_realign on FP8 pages return
- * SP_ERR_UNSUPPORTED. */
+ * FP8 pages need head_dim 128.  Decode and prefill read them: decode with
+ * f16 MMAs (see sp_set_kv_scales), prefill by turning each history tile into
+ * bf16(code * scale) rows in shared memory before its bf16 MMAs (a chunk's
+ * own rows enter its attention as the caller's bf16 values).
+ * sp_rope_realign on FP8 pages returns SP_ERR_UNSUPPORTED. */
 typedef enum { SP_KV_BF16 = 0, SP_KV_FP8_E4M3 = 1 } sp_kv_dtype;
 
 typedef struct sp_cache sp_cache;  /* opaque host handle */

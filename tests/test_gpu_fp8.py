@@ -145,41 +145,70 @@ def test_append_steps_long_context():
     assert cache.status() == 0
 
 
-def test_prefill_without_history_then_refusals():
-    """A first chunk prefills over its own bf16 K/V; its write stores codes;
-    a chunk over FP8 history and RoPE realignment are refused, changing
-    nothing."""
+@pytest.mark.parametrize("P,n,c2", [(64, 700, 300), (16, 1500, 200), (128, 5000, 129), (32, 33, 640)])
+def test_prefill_first_chunk_then_over_fp8_history(P, n, c2):
+    """A first chunk prefills over its own bf16 K/V and its write stores
+    codes; the next chunk attends over the FP8 history (dequantised by the
+    oracle) plus its own bf16 rows.  RoPE realignment of FP8 pages is
+    refused and changes nothing."""
     gpu_ready()
     from head_aware_paged_gb300 import SegPagedError
-    hq, hkv, P, n = 16, 4, 64, 700
-    cache = _mk(hq, hkv, P, 2, 2048, 200)
+    hq, hkv = 16, 4
+    tot = n + c2
+    cache = _mk(hq, hkv, P, 2, 2 * tot + 64, 2 * hkv * ((tot + 64) // P + 3))   # max_tokens >= both chunks
     pols = [W.HeadPolicy(G), W.HeadPolicy(L, 4, 100), W.HeadPolicy(G),
-            W.HeadPolicy(R, idx=np.arange(3, 2000, 5, dtype=np.int32))]
+            W.HeadPolicy(R, idx=np.arange(3, tot, 5, dtype=np.int32))]
     cache.set_policy(0, to_c_policies([pols]))
     cache.set_policy(1, to_c_policies([pols]))
-    q = W.normal((2 * n, hq, D), 1, device="cuda")
-    k, v = _outlier_kv(2 * n, hkv, 2)
+    q = W.normal((2 * tot, hq, D), 1 + P, device="cuda")
+    k, v = _outlier_kv(2 * tot, hkv, 2 + P)
     ks, vs = _scales(k), _scales(v)
     cache.set_kv_scales(0, ks, vs)
-    out, lse = cache.prefill(0, [0, 1], [0, n, 2 * n], q, k, v)
-    torch.cuda.synchronize()
     pt = [pol_tuple(p) for p in pols]
+    # first chunk: rows 0..n-1 of both sequences (sequence b uses rows b*tot ..)
+    r1 = torch.cat([torch.arange(b * tot, b * tot + n) for b in range(2)]).cuda()
+    q1, k1, v1 = q[r1].contiguous(), k[r1].contiguous(), v[r1].contiguous()
+    out, lse = cache.prefill(0, [0, 1], [0, n, 2 * n], q1, k1, v1)
+    torch.cuda.synchronize()
     for b in range(2):
         sl = slice(b * n, (b + 1) * n)
-        ref, lref = oracle.attend(f64(q[sl]), f64(k[sl]), f64(v[sl]), list(range(n)), pt, "f64",
+        ref, lref = oracle.attend(f64(q1[sl]), f64(k1[sl]), f64(v1[sl]), list(range(n)), pt, "f64",
                                   threads=ncores())
         compare(out[sl], ref, lse[sl], lref, "fp8 first chunk %d" % b)
-    cache.append_kv(0, [0, 1], [0, n, 2 * n], k, v)
+    cache.append_kv(0, [0, 1], [0, n, 2 * n], k1, v1)
     torch.cuda.synchronize()
     for b in range(2):
         sl = slice(b * n, (b + 1) * n)
-        assert sum(_check_codes(cache, b, 0, h, k[sl], v[sl], ks, vs) for h in range(hkv)) > 0
+        assert sum(_check_codes(cache, b, 0, h, k1[sl], v1[sl], ks, vs) for h in range(hkv)) > 0
+    # second chunk over the FP8 history
+    r2 = torch.cat([torch.arange(b * tot + n, (b + 1) * tot) for b in range(2)]).cuda()
+    q2, k2, v2 = q[r2].contiguous(), k[r2].contiguous(), v[r2].contiguous()
+    out2, lse2 = cache.prefill(0, [0, 1], [0, c2, 2 * c2], q2, k2, v2)
+    torch.cuda.synchronize()
+    for b in range(2):
+        hist = slice(b * tot, b * tot + n)
+        kk = np.concatenate([_dq(k[hist], ks), f64(k2[b * c2:(b + 1) * c2])], axis=0)
+        vv = np.concatenate([_dq(v[hist], vs), f64(v2[b * c2:(b + 1) * c2])], axis=0)
+        sl = slice(b * c2, (b + 1) * c2)
+        ref, lref = oracle.attend(f64(q2[sl]), kk, vv, list(range(n, tot)), pt, "f64", threads=ncores())
+        compare(out2[sl], ref, None, None, "fp8 history chunk %d" % b)
+        # The history rows enter the bf16 MMAs as bf16(code * scale): each
+        # score moves by at most 2^-9 sum_i |q_i k_i| / sqrt(d) (twice that
+        # as slack), and so does the log-sum-exp
+        qa = np.abs(f64(q2[sl]))                              # [c2, hq, d]
+        ka = np.abs(kk[:n])                                   # [n, hkv, d]
+        grp = hq // hkv
+        bound = np.stack([(qa[:, h] @ ka[:, h // grp].T).max(axis=1) for h in range(hq)], axis=1)
+        bound = 2.0 ** -8 * bound / np.sqrt(D) + 2e-3
+        lg = lse2[sl].cpu().numpy().astype(np.float64)
+        fin = np.isfinite(lref)
+        assert np.array_equal(np.isfinite(lg), fin)
+        assert (np.abs(lg - lref)[fin] <= bound[fin]).all(), np.abs(lg - lref)[fin].max()
+    assert cache.status() == 0
     pool0 = cache.k_pool().clone()
     with pytest.raises(SegPagedError):
-        cache.prefill(0, [0], [0, 10], q[:10], k[:10], v[:10])
-    with pytest.raises(SegPagedError):
         cache.rope_realign(0, [0], 5)
-    assert cache.seq_len(0, 0) == n and torch.equal(cache.k_pool(), pool0)
+    assert torch.equal(cache.k_pool(), pool0)
     assert cache.status() == 0
 
 
