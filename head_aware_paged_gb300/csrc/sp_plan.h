@@ -220,16 +220,5 @@ SP_HD bool key_visible(const KvTile& k, const UnitPol& u, I i, int c, I table_po
     return true;
 }
 
-// Work estimate of an item (keys times MMA width), for ordering.
-SP_HD int64_t plan_cost(const Plan& pl) {
-    int64_t c = 0;
-    for (int s = 0; s < kMaxSegs; ++s) {
-        if (pl.seg[s].len <= 0) continue;
-        const int64_t full_tiles = pl.seg[s].len / kTileKeys;
-        const int64_t rest = pl.seg[s].len - full_tiles * kTileKeys;
-        c += full_tiles * kTileKeys + ((rest + 15) & ~15) + (rest > 0 ? 32 : 0) + 32 * full_tiles;
-    }
-    return c;
-}
 
 }  // namespace sp

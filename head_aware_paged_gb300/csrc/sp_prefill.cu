@@ -62,6 +62,8 @@ constexpr int kSmemLimit = 232448;     // 227 KB per CTA
 constexpr int kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;   // lazy-rescale threshold (log2 units)
 constexpr int kPrefetchTiles = 3;      // K/V tiles brought into L2 ahead of their loads
+constexpr int64_t kTileCost = 160;     // work-assignment cost of one K/V tile
+constexpr int64_t kItemCost = 480;     // and of one work item's fixed part
 
 struct PrefillParams {
     Meta meta;
@@ -813,7 +815,12 @@ sp_status prefill_impl(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32
                 const int64_t i_lo = n_b + rb * 128;
                 const int64_t i_hi = n_b + std::min(cb, rb * 128 + 128) - 1;
                 const Plan pl = make_plan(u, idx, n_b, i_lo, i_hi, P);
-                const int64_t cost = plan_cost(pl) + 64;
+                // Time model for the assignment, measured per CTA with clock64
+                // traces: every K/V tile costs about the same whatever its
+                // width (the softmax treats a whole tile), and an item adds the
+                // pipeline fill, the epilogue and the hand-over to the next
+                // item, about three tiles' worth.
+                const int64_t cost = kTileCost * pl.ntiles + kItemCost;
                 for (int pr = 0; pr < pairs; ++pr)
                     cands.push_back({cost, make_int4(b, h, pr | (rb << 8), (int)pl.ntiles)});
             }
