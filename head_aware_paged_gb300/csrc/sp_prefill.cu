@@ -65,6 +65,7 @@ constexpr int kPrefetchTiles = 3;      // K/V tiles brought into L2 ahead of the
 constexpr int64_t kTileCost = 160;     // work-assignment cost of one K/V tile
 constexpr int64_t kItemCost = 480;     // and of one work item's fixed part
 
+constexpr int kInlineWords = 1344;     // int4 words of work list carried in the parameters
 struct PrefillParams {
     Meta meta;
     Geo geo;
@@ -80,6 +81,13 @@ struct PrefillParams {
     int32_t n_b[kMaxCallSeqs];   // tokens held before the chunk
     int32_t cnt[kMaxCallSeqs];   // chunk rows
     int32_t row0[kMaxCallSeqs];  // first chunk row in q / k / v
+    // A work list that fits travels inside the parameters (items, then the
+    // CTA offsets as int32 packed four to an int4); inline_words = 0 means
+    // it was uploaded to items / cta_off.  Inline, the launch carries it and
+    // no copy engine is involved, so the kernel never queues behind the
+    // caller's own host<->device transfers.
+    int32_t inline_words;
+    int4 inl[kInlineWords];
 };
 
 template <int D, bool F8 = false>
@@ -108,8 +116,8 @@ struct Item {
     const int32_t* ptab;
 };
 
-__device__ __forceinline__ Item load_item(const PrefillParams& p, int n) {
-    const int4 it = p.items[n];
+__device__ __forceinline__ Item load_item(const PrefillParams& p, const int4* items, int n) {
+    const int4 it = items[n];
     Item m;
     m.b = it.x;
     m.kvh = it.y;
@@ -210,6 +218,10 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
     const int G = gridDim.x, cta = blockIdx.x;
     const Geo& g = p.geo;
     const int nq = p.nq;
+    // the work list: in the parameters (generic loads of the parameter
+    // space; no __ldg there) or in the workspace
+    const int4* items = p.inline_words ? p.inl : p.items;
+    const int32_t* cta_off = p.inline_words ? reinterpret_cast<const int32_t*>(p.inl + p.n_items) : p.cta_off;
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
@@ -243,8 +255,8 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
         prefetch_tmap(&tmKp); prefetch_tmap(&tmVp);
         uint32_t q_loads = 0, L = 0, F = 0;     // F: FP8 code slots filled
         bool ok = true;
-        for (int n = p.cta_off[cta]; n < p.cta_off[cta + 1] && ok; ++n) {
-            const Item it = load_item(p, n);
+        for (int n = cta_off[cta]; n < cta_off[cta + 1] && ok; ++n) {
+            const Item it = load_item(p, items, n);
             const Plan pl = make_plan(it.pol, it.idx, it.n_b, it.i_lo, it.i_hi, P);
             if (pl.ntiles == 0) continue;
             if (q_loads > 0 && !mbar_wait(q_empty, (q_loads - 1) & 1, abort_flag, status)) { ok = false; break; }
@@ -257,8 +269,8 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
             // L2 prefetch: the next item's Q now, and K/V tiles kPrefetchTiles
             // ahead of their loads (HBM latency is longer than the stage ring
             // can cover on its own)
-            if (n + 1 < p.cta_off[cta + 1]) {
-                const Item nx = load_item(p, n + 1);
+            if (n + 1 < cta_off[cta + 1]) {
+                const Item nx = load_item(p, items, n + 1);
                 for (int t = 0; t < nq; ++t)
                     for (int hf = 0; hf < S::kHalves; ++hf)
                         tma_prefetch_2d(&tmQ, (nx.h0 + t) * D + hf * 64, (int32_t)nx.row_base);
@@ -407,9 +419,9 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
         // the stage, so between two tiles this thread only waits and issues.
         uint32_t q_uses = 0, L = 0, e = 0, tiles = 0;   // both query tiles see every K/V tile
         bool ok = true;
-        const int n_end = p.cta_off[cta + 1];
-        for (int n = p.cta_off[cta]; n < n_end && ok; ++n) {
-            const int nt = __ldg(&p.items[n].w);
+        const int n_end = cta_off[cta + 1];
+        for (int n = cta_off[cta]; n < n_end && ok; ++n) {
+            const int nt = items[n].w;
             if (nt == 0) continue;
             if (!mbar_wait(q_full, q_uses & 1, abort_flag, status)) { ok = false; break; }
             ++q_uses;
@@ -528,8 +540,8 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
             const float sl2 = p.scale_log2;
             uint32_t k = 0;
             bool ok = true;
-            for (int n = p.cta_off[cta]; n < p.cta_off[cta + 1] && ok; ++n) {
-                const Item it = load_item(p, n);
+            for (int n = cta_off[cta]; n < cta_off[cta + 1] && ok; ++n) {
+                const Item it = load_item(p, items, n);
                 const Plan pl = make_plan(it.pol, it.idx, it.n_b, it.i_lo, it.i_hi, P);
                 const int head = it.h0 + t;
                 const bool row_ok = r < it.rows;
@@ -751,6 +763,11 @@ __global__ void k_prefill_counts(Meta meta, Geo g, int seq, int layer, int h,
     }
 }
 
+// the parameters (work list included) and the five tensor maps must fit the
+// kernel parameter space (32,764 bytes)
+static_assert(sizeof(PrefillParams) + 5 * sizeof(CUtensorMap) <= 32764,
+              "prefill parameters exceed the kernel parameter space");
+
 template <int D, int P, bool F8 = false>
 cudaError_t launch_prefill_t(sp_cache* c, const PrefillParams& p, int grid,
                              const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -847,13 +864,15 @@ sp_status prefill_impl(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32
             heap.push(top);
         }
     }
-    // one upload: the items grouped by CTA, then the CTA offsets, through the
-    // next pinned staging buffer (asynchronous; waits only if that buffer's
-    // previous copy has not run yet)
+    // The items grouped by CTA, then the CTA offsets: inside the kernel
+    // parameters when they fit, else one upload through the next pinned
+    // staging buffer (asynchronous; waits only if that buffer's previous
+    // copy has not run yet)
     const size_t n_items = cands.size();
     const size_t words = n_items + (grid + 1 + 3) / 4;
+    const bool inl = words <= (size_t)kInlineWords;
     int si = -1;
-    int4* buf = static_cast<int4*>(stage_acquire(c, words * sizeof(int4), &si));
+    int4* buf = inl ? p.inl : static_cast<int4*>(stage_acquire(c, words * sizeof(int4), &si));
     if (!buf) return fail(SP_ERR_CUDA, "prefill staging buffer");
     int32_t* off = reinterpret_cast<int32_t*>(buf + n_items);
     size_t pos = 0;
@@ -862,11 +881,15 @@ sp_status prefill_impl(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32
         for (const int4& it : per[g2]) buf[pos++] = it;
     }
     off[grid] = (int32_t)pos;
-    p.items = c->ws.tiles;
-    p.cta_off = reinterpret_cast<const int32_t*>(c->ws.tiles + n_items);
     p.n_items = (int32_t)n_items;
-    cudaError_t e = stage_copy(c, si, c->ws.tiles, words * sizeof(int4), stream);
-    if (e != cudaSuccess) return cuda_fail(e, "prefill work list upload");
+    p.inline_words = inl ? (int32_t)words : 0;
+    cudaError_t e = cudaSuccess;
+    if (!inl) {
+        p.items = c->ws.tiles;
+        p.cta_off = reinterpret_cast<const int32_t*>(c->ws.tiles + n_items);
+        e = stage_copy(c, si, c->ws.tiles, words * sizeof(int4), stream);
+        if (e != cudaSuccess) return cuda_fail(e, "prefill work list upload");
+    }
     CUtensorMap tq, tk, tv;
     std::string err;
     const int D = c->cfg.head_dim;
