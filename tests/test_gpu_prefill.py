@@ -218,3 +218,31 @@ def test_llama33_70b_shape_sampled():
     ref, lref = oracle.attend(f64(q[rows]), f64(k), f64(v), rows, pt, "f64", threads=ncores())
     compare(out[rows], ref, lse[rows], lref, "llama-70B-shaped layer %d" % layer)
     assert cache.status() == 0
+
+
+def test_work_list_in_parameters_or_uploaded_gives_identical_rows():
+    """A call whose work list fits the kernel parameters (one 8192-row
+    sequence, Hq 32 / Hkv 8: 1024 items) and a call that uploads it (the same
+    sequence batched with a second one: 2048 items) compute every item the
+    same way, whichever CTA runs it: the first sequence's rows are bitwise
+    equal, and sampled rows of both match the oracle."""
+    gpu_ready()
+    wl = W.WORKLOADS["mistral7b_prefill_8k"]
+    Lq = wl.seq_len
+    pols = W.policies(wl)
+    cache = _mk(1, wl.hq, wl.hkv, wl.d, wl.page, 2, Lq, 800, max_tokens=2 * Lq)
+    cache.set_policy(0, to_c_policies(pols))
+    cache.set_policy(1, to_c_policies(pols))
+    q, k, v = W.qkv(wl, 2 * Lq, 0, 0, device="cuda")
+    alone, lse_a = cache.prefill(0, [0], [0, Lq], q[:Lq].contiguous(), k[:Lq].contiguous(),
+                                 v[:Lq].contiguous())
+    both, lse_b = cache.prefill(0, [0, 1], [0, Lq, 2 * Lq], q, k, v)
+    torch.cuda.synchronize()
+    assert torch.equal(alone, both[:Lq]) and torch.equal(lse_a, lse_b[:Lq])
+    pt = [pol_tuple(p) for p in pols[0]]
+    rows = np.array([0, 1, 127, 128, 1000, 4095, 4096, Lq - 1])
+    for b in range(2):
+        kb, vb = f64(k[b * Lq:(b + 1) * Lq]), f64(v[b * Lq:(b + 1) * Lq])
+        ref, lref = oracle.attend(f64(q[b * Lq + rows]), kb, vb, rows, pt, "f64", threads=ncores())
+        compare(both[b * Lq + rows], ref, lse_b[b * Lq + rows], lref, "batched sequence %d" % b)
+    assert cache.status() == 0
