@@ -250,6 +250,12 @@ def sp_get_status(handle, stream=None) -> int:
     return w.value
 
 
+def sp_selftest_bounded_wait(handle, limit_cycles: int, mode: int, stream=None) -> None:
+    """Launch the bounded-wait self-test (mode 0: the wait gives up and the
+    next status read reports SP_ERR_TIMEOUT; mode 1: the wait completes)."""
+    check(load().sp_selftest_bounded_wait(handle, limit_cycles, mode, _stream(stream)))
+
+
 def sp_last_error() -> str:
     return load().sp_last_error().decode(errors="replace")
 

@@ -18,7 +18,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libsegpaged.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["sp_api.cu", "sp_storage.cu", "sp_decode.cu", "sp_prefill.cu", "sp_decode_static.cu",
-           "sp_rope.cu", "sp_transfer.cu", "sp_select.cu"]
+           "sp_rope.cu", "sp_transfer.cu", "sp_select.cu", "sp_selftest.cu"]
 
 
 def nvcc() -> str:

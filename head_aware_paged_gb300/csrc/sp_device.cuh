@@ -53,13 +53,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // time-out it raises *abort and the device status word.  Returns false when
 // it gave up.  Never spins without a limit.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          volatile int* abort, int* status) {
+                                          volatile int* abort, int* status,
+                                          long long limit = kWaitCycles) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (abort && *abort) return false;
-        if (clock64() - t0 > kWaitCycles) {
+        if (clock64() - t0 > limit) {
             if (abort) *abort = 1;
             if (status) atomicOr(status, kStatusTimeout);
             return false;

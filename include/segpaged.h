@@ -335,6 +335,16 @@ sp_status sp_count_decode_bytes(const sp_cache* cache, int32_t layer,
  * word is then cleared).  *word (nullable) receives the raw flags. */
 sp_status sp_get_status(sp_cache* cache, void* stream, int32_t* word);
 
+/* Check of the bounded waits every kernel uses (no fault, no hang): one
+ * warp waits on a shared-memory mbarrier for at most limit_cycles
+ * ([1000, 2e9] clock cycles).  mode 0: nothing arrives, the wait gives up and
+ * raises the timeout flag of the cache's status word, so the next
+ * sp_get_status returns SP_ERR_TIMEOUT (and clears it); mode 1: a second
+ * warp arrives after limit_cycles / 8 and the status stays clear.
+ * Asynchronous on `stream`; SP_ERR_INVALID_ARG for other arguments. */
+sp_status sp_selftest_bounded_wait(sp_cache* cache, int64_t limit_cycles, int32_t mode,
+                                   void* stream);
+
 /* Message of the last failing call on this thread ("" if none). */
 const char* sp_last_error(void);
 
