@@ -12,12 +12,13 @@
 //     splits that list evenly: CTA c streams items [T c / G, T (c+1) / G), so
 //     every SM reads the same number of pages whatever the head classes.
 //   * One producer lane streams the pages with 2D TMA loads (128-byte
-//     swizzle) into a ring of shared-memory stages; four consumer warps share
-//     each page (16 keys each) and compute QK^T and PV for all query heads of
-//     the KV head at once with mma.sync m16n8k16 (rows = query heads, so each
-//     K/V byte is read once for the whole GQA group), with an online softmax
-//     in registers (tutorial section 10.2) and deferred normalisation
-//     (section 10.4).
+//     swizzle) into a ring of shared-memory stages; each stage belongs to one
+//     of the consumer warps, which takes the whole page (blocks of 32 keys)
+//     and computes QK^T and PV for all query heads of the KV head at once
+//     with mma.sync m16n8k16 (rows = query heads, so each K/V byte is read
+//     once for the whole GQA group), with an online softmax in registers
+//     (tutorial section 10.2) and deferred normalisation (section 10.4).
+//     The warps' partial states are merged at the end of each unit.
 //   * Where a unit's items span several CTAs (split-KV), each CTA writes an
 //     unnormalised partial (o, m, l); the last CTA to finish the unit (atomic
 //     ticket, no waiting) merges them: m* = max m_s, l* = sum 2^(m_s-m*) l_s,
@@ -31,9 +32,7 @@ namespace {
 
 constexpr int kConsumerWarps = 4;
 constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
-constexpr int kMaxGroup = 16;
 constexpr int kMaxStages = 8;
-constexpr int kItemFirst = 1, kItemLast = 2;   // item flags: first / last of its unit in a CTA
 
 template <int D, int P, bool F8 = false>
 struct DecodeShape {
@@ -48,9 +47,9 @@ struct DecodeShape {
     // Shared memory a CTA may use: all of an SM's, or half of it for two CTAs.
     // The stages get what the merge buffers (sized by the call's group and
     // grid) and the barriers leave, up to kMaxStages; bf16 stages are capped
-    // at 160 KB (deeper rings measured no faster).
+    // at 192 KB (six 32 KB stages at P = 64, owned by three warps).
     static constexpr int kSmemCap = F8 ? 113 * 1024 : 227 * 1024;
-    static constexpr int kStageCap = F8 ? kSmemCap : 160 * 1024;
+    static constexpr int kStageCap = F8 ? kSmemCap : 192 * 1024;
     static constexpr int kMiscBytes = kMaxStages * 16 /*full, empty*/ + kMaxStages * 16 /*desc*/
                                       + 16 /*flags*/ + 32 * 16 /*producer batch*/
                                       + 16 /*barrier alignment*/ + 1024 /*base alignment*/;
@@ -93,7 +92,7 @@ k_decode(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtenso
     const int group = g.group;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NST; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], kConsumerWarps); }
+        for (int s = 0; s < NST; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }   // one consumer warp per page
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -142,10 +141,7 @@ k_decode(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtenso
                         atomicOr(p.meta.status, kStatusBadPage);
                         page = 0; lo = hi = 0;          // load something harmless, use nothing
                     }
-                    // first / last item of its unit in this CTA's stream
-                    const int fl = ((x == x0 || p.item_off[u] == x) ? kItemFirst : 0) |
-                                   ((x + 1 == x1 || p.item_off[u + 1] == x + 1) ? kItemLast : 0);
-                    batch[lane] = make_int4(u, (int)lo | ((int)hi << 16), page, fl);
+                    batch[lane] = make_int4(u, (int)lo | ((int)hi << 16), page, 0);
                 }
                 __syncwarp();
                 if (lane == 0) {
@@ -200,17 +196,30 @@ k_decode(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtenso
     uint32_t qa[D / 16][4];
     float m_run[2], l_run[2];
     float o_acc[D / 8][4];
-    int b = 0, h = 0;
-    int s = 0;                        // stage of the next item
-    uint32_t ks = 0;                  // times that stage has been filled before
-
-    for (int xi = 0; xi < (int)(x1 - x0); ++xi) {
-        if (!mbar_wait(&full[s], ks & 1, abort_flag, p.meta.status)) break;
-        const int4 dd = desc[s];
-        const int u = dd.x, lo = dd.y & 0xFFFF, hi = dd.y >> 16, fl = dd.z;
-        if (fl & kItemFirst) {
-            b = u / g.hkv;
-            h = u - b * g.hkv;
+    // Consumer warp w < W takes items w, w+W, w+2W, ... of this CTA's stream
+    // (whole pages), so a warp only handles the pages it computes.  W divides
+    // the stage count (the launcher makes NST a multiple of 4, or W = NST
+    // below 4 stages), so stage s always belongs to warp s % W and each warp
+    // waits for its stages' fills in order -- never for a fill two phases
+    // ahead.  All four warps walk the same list of units and merge at the
+    // end of each, whatever their own pages were; after a failed wait a warp
+    // only keeps walking, so that every merge barrier still sees all four.
+    const int W = p.owners;
+    const bool owner = warp < W;
+    int xi = warp;                    // this warp's next item, relative to x0
+    int s = warp;                     // its stage (xi % NST)
+    uint32_t rounds = 0;              // times that stage has been filled before
+    bool dead = false;
+    int u_lo = 0, u_hi = p.n_units - 1;     // first unit with an item >= x0
+    while (u_lo < u_hi) {
+        const int mid = (u_lo + u_hi) >> 1;
+        if (p.item_off[mid + 1] <= x0) u_lo = mid + 1; else u_hi = mid;
+    }
+    for (int u = u_lo; u < p.n_units && p.item_off[u] < x1; ++u) {
+        const int64_t ua = max64(p.item_off[u], x0), ub = min64(p.item_off[u + 1], x1);
+        if (ua >= ub) continue;       // no pages (handled above) or none in this CTA
+        const int b = u / g.hkv, h = u - (u / g.hkv) * g.hkv;
+        {
             const __nv_bfloat16* qb = p.q + ((int64_t)b * g.hq + h * group) * D;
             auto ld = [&](int r, int cc) -> uint32_t {
                 return r < group ? *reinterpret_cast<const uint32_t*>(qb + (int64_t)r * D + cc) : 0u;
@@ -252,14 +261,18 @@ k_decode(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtenso
                 #pragma unroll
                 for (int e = 0; e < 4; ++e) o_acc[nt][e] = 0.f;
         }
+        for (; owner && x0 + xi < ub; xi += W) {
+        if (!dead && !mbar_wait(&full[s], rounds & 1, abort_flag, p.meta.status)) dead = true;
+        if (dead) continue;
+        const int4 dd = desc[s];
+        const int lo = dd.y & 0xFFFF, hi = dd.y >> 16;
+        if (dd.x != u && lane == 0) atomicOr(p.meta.status, kStatusBadState);
         const uint32_t kbase = smem_u32(stages + s * S::kStageBytes);
         const uint32_t vbase = kbase + S::kTileBytes;
-        // Blocks of BK keys go to the consumer warps round robin along this
-        // CTA's item stream (block i of item x is block (x - x0) * NB + i),
-        // so every warp has work whatever the page size.
-        const int blk = (warp - ((xi * NB) & 3)) & 3;
+        #pragma unroll 1
+        for (int blk = 0; blk < NB; ++blk) {
         const int key0 = blk * BK;
-        if (blk < NB && key0 < hi && key0 + BK > lo) {
+        if (key0 < hi && key0 + BK > lo) {
             // S = Q K^T for BK keys: NT n-tiles of 8 keys
             float sc[NT][4];
             #pragma unroll
@@ -409,10 +422,12 @@ k_decode(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtenso
                 }
             }
         }
+        }   // blocks of the page
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
-        if (++s == NST) { s = 0; ++ks; }
-        if (!(fl & kItemLast)) continue;
+        s += W;
+        if (s >= NST) { s -= NST; ++rounds; }
+        }   // this warp's pages of the unit
 
         // ------------- merge the four warps' partial states -------------
         #pragma unroll
@@ -564,7 +579,13 @@ cudaError_t launch_decode_t(const sp_cache* c, DecodeParams& p, int grid, cudaSt
     p.merge_floats = (mo + 3) & ~3;
     const int merge_bytes = (p.merge_floats + kConsumerWarps * group * 2) * 4;
     const int room = std::min(Sh::kStageCap, Sh::kSmemCap - merge_bytes - Sh::kMiscBytes);
-    p.nst = std::min(kMaxStages, room / Sh::kStageBytes);
+    // the deepest ring whose stages split evenly over at least three warps
+    // (or over all of them when there are fewer than three stages)
+    p.nst = 0;
+    for (int n = std::min(kMaxStages, room / Sh::kStageBytes); n >= 2 && p.nst == 0; --n) {
+        const int w = n % 4 == 0 ? 4 : n % 3 == 0 ? 3 : n % 2 == 0 ? 2 : 1;
+        if (w >= std::min(3, n)) { p.nst = n; p.owners = w; }
+    }
     if (p.nst < 2) return cudaErrorInvalidConfiguration;
     const int smem = p.nst * Sh::kStageBytes + merge_bytes + Sh::kMiscBytes;
     cudaError_t e = cudaFuncSetAttribute(k_decode<D, P, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,

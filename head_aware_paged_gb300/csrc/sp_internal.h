@@ -70,6 +70,7 @@ struct DecodeParams {
     int32_t* counters;           // [n_units], zero between calls
     float scale_log2;            // log2(e) / sqrt(d)
     int32_t nst;                 // pipeline stages (set by the launcher)
+    int32_t owners;              // consumer warps that own stages (divides nst)
     int32_t merge_floats;        // merge buffer floats (set by the launcher)
 };
 
