@@ -336,6 +336,70 @@ class DecodeStep:
         return sum(self.cache.count_decode_bytes(l, self.seqs, [t] * self.B)
                    for l in range(self.layers))
 
+    # host-buffer (end-to-end) variant: each layer's q / new k / new v come
+    # from pinned host memory (one packed copy per layer) and its out / lse
+    # go back (one packed copy); uploads, kernels and downloads run on three
+    # streams, so layer l+1's upload and layer l-1's download overlap layer
+    # l's kernels
+    def setup_e2e(self):
+        import torch
+        nq, nk = self.qs.numel(), self.kn.numel()
+        self.e2e_split = (nq, nq + nk, nq + 2 * nk)
+        packed = torch.cat([self.qs.reshape(-1), self.kn.reshape(-1), self.vn.reshape(-1)])
+        self.h_in = packed.cpu().pin_memory()
+        self.d_in = [torch.empty_like(packed) for _ in range(self.layers)]
+        no, nl = self.out.numel(), self.lse.numel()      # out bf16, lse fp32 (2 bf16 slots each)
+        self.d_out = [torch.empty(no + 2 * nl, dtype=torch.bfloat16, device=packed.device)
+                      for _ in range(self.layers)]
+        self.h_out = [torch.empty(no + 2 * nl, dtype=torch.bfloat16).pin_memory() for _ in range(self.layers)]
+        self.streams = [torch.cuda.Stream() for _ in range(3)]
+        self.ev = {k: [torch.cuda.Event() for _ in range(self.layers)] for k in ("in", "done", "out")}
+        self.h2d_bytes = packed.numel() * 2 * self.layers
+        self.d2h_bytes = (no + 2 * nl) * 2 * self.layers
+
+    def run_e2e_steps(self, n):
+        """n decode steps through the C ABI with host buffers; returns (CUDA
+        events around all of them, visible bytes they read)."""
+        import torch
+        sh, sc, sd = self.streams
+        cur = torch.cuda.current_stream()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(cur)
+        for st_ in self.streams:
+            st_.wait_event(start)
+        a, b, e = self.e2e_split
+        no = self.out.numel()
+        work = 0
+        for step in range(n):
+            work += self.step_bytes(self.t)
+            for l in range(self.layers):
+                din, dout = self.d_in[l], self.d_out[l]
+                q = din[:a].view(self.qs.shape)
+                kn = din[a:b].view(self.kn.shape)
+                vn = din[b:e].view(self.vn.shape)
+                out = dout[:no].view(self.out.shape)
+                lse = dout[no:].view(torch.float32).view(self.lse.shape)
+                with torch.cuda.stream(sh):
+                    if step > 0:
+                        sh.wait_event(self.ev["done"][l])     # last step's kernels read din
+                    din.copy_(self.h_in, non_blocking=True)
+                    self.ev["in"][l].record(sh)
+                sc.wait_event(self.ev["in"][l])
+                if step > 0:
+                    sc.wait_event(self.ev["out"][l])         # last step's outputs are home
+                self.cache.append_kv(l, self.seqs, self.cu, kn, vn, stream=sc)
+                self.cache.decode(l, self.seqs, q, out, lse, stream=sc)
+                self.ev["done"][l].record(sc)
+                sd.wait_event(self.ev["done"][l])
+                with torch.cuda.stream(sd):
+                    self.h_out[l].copy_(dout, non_blocking=True)
+                    self.ev["out"][l].record(sd)
+            self.t += 1
+        for st_ in self.streams:
+            cur.wait_stream(st_)
+        end.record(cur)
+        return start, end, work
+
     def run(self, ev_pf=None):
         c = self.cache
         for l in range(self.layers):
@@ -465,32 +529,15 @@ def run_ours(args, ws, rank):
         e2e = {"value": ws * st.work * e2e_steps * scale / (e2e_ms / 1e3), "unit": st.unit,
                "h2d_bytes_per_step": st.h2d_bytes, "d2h_bytes_per_step": st.d2h_bytes}
     else:
-        bytes_in = (st.qs.numel() + st.kn.numel() + st.vn.numel()) * 2 * st.layers   # bf16 inputs
-        bytes_out = (st.out.numel() * 2 + st.lse.numel() * 4) * st.layers
-        hq_ = st.qs.cpu().pin_memory()
-        hk_ = st.kn.cpu().pin_memory()
-        hv_ = st.vn.cpu().pin_memory()
-        ho = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
-        hl = torch.empty(st.lse.shape, dtype=st.lse.dtype).pin_memory()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e2e_steps = 3
-        w = 0
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            w += st.step_bytes(st.t)
-            c = st.cache
-            for l in range(st.layers):
-                st.qs.copy_(hq_, non_blocking=True)
-                st.kn.copy_(hk_, non_blocking=True)
-                st.vn.copy_(hv_, non_blocking=True)
-                c.append_kv(l, st.seqs, st.cu, st.kn, st.vn)
-                c.decode(l, st.seqs, st.qs, st.out, st.lse)
-                ho.copy_(st.out, non_blocking=True)
-                hl.copy_(st.lse, non_blocking=True)
-            st.t += 1
-        e1.record(stream)
+        st.setup_e2e()
+        st.run_e2e_steps(1)
         torch.cuda.synchronize()
+        barrier(ws)
+        e0, e1, w = st.run_e2e_steps(3)
+        torch.cuda.synchronize()
+        assert st.cache.status() == 0
         e2e_ms = reduce_max(e0.elapsed_time(e1), ws)
+        bytes_in, bytes_out = st.h2d_bytes, st.d2h_bytes
         e2e = {"value": ws * w * scale / (e2e_ms / 1e3), "unit": st.unit,
                "h2d_bytes_per_step": bytes_in, "d2h_bytes_per_step": bytes_out}
 
