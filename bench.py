@@ -703,9 +703,10 @@ def run_op_rope(args):
     2 * 2d bytes per rotated row (read + write)."""
     import torch
     wl = W.WORKLOADS["llama3_8b_decode_32k"]
-    st = DecodeStep(wl, layers=1)
+    fp8 = args.kv_dtype == "fp8"
+    st = DecodeStep(wl, layers=1, fp8=fp8)
     c = st.cache
-    nbytes = stored_rows(st.pols[0], st.n, st.B, wl.page) * 2 * wl.d * 2
+    nbytes = stored_rows(st.pols[0], st.n, st.B, wl.page) * 2 * wl.d * (1 if fp8 else 2)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
     for _ in range(args.warmup):
         c.rope_realign(0, st.seqs, 1000)
@@ -733,8 +734,9 @@ def run_op_rope(args):
     return {"metric": "RoPE realignment of stored K rows, GB/s moved (read + write)",
             "op": "rope_realign", "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total / args.steps, "higher_is_better": True,
-            "dtype": "bf16", "data": "synthetic (seeded N(0,1), pages' shapes)",
-            "config": {"workload": "llama3_8b_decode_32k, layer 0, all 32 sequences",
+            "dtype": "e4m3 K pages (fp32 rotation)" if fp8 else "bf16",
+            "data": "synthetic (seeded N(0,1), pages' shapes)",
+            "config": {"workload": "llama3_8b_decode_32k%s, layer 0, all 32 sequences" % ("_fp8" if fp8 else ""),
                        "bytes_per_call": nbytes, "l2": "flushed between calls"},
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                          "frac": gbs / peak, "traffic": None, "kernel": "k_rope",

@@ -646,7 +646,6 @@ sp_status sp_rope_realign(sp_cache* c, int32_t layer, const int32_t* seq_ids, in
         return fail(SP_ERR_INVALID_ARG, "rope_theta must be positive and finite");
     if (delta < -(int64_t(1) << 40) || delta > (int64_t(1) << 40))
         return fail(SP_ERR_INVALID_ARG, "delta out of range (|delta| <= 2^40)");
-    if (c->geo.fp8) return fail(SP_ERR_UNSUPPORTED, "RoPE realignment of FP8 pages is not built");
     if (pos_lo == pos_hi || delta == 0) return SP_OK;   // nothing moves
     std::unique_ptr<RopeParams> pp(new RopeParams());
     RopeParams& p = *pp;

@@ -52,15 +52,63 @@ __device__ __forceinline__ void rotate8(uint4& xa, uint4& yb, const float* cs, c
     yb = make_uint4(yw[0], yw[1], yw[2], yw[3]);
 }
 
+// FP8 pages: 16 pairs held as e4m3 codes (x: elements i .. i+15, y: i+d/2 ..
+// i+d/2+15).  Each element is dequantised with its channel's K scale, the
+// pair rotated in fp32 with every product and sum rounded separately (no
+// fused multiply-add, so the result is one fixed sequence of roundings) and
+// requantised like a write: e4m3(v * fp32(1 / scale)), nearest even,
+// saturating.
+__device__ __forceinline__ float f32_of_e4m3(uint32_t code) {
+    const uint32_t h2 = f16x2_of_e4m3x2(code & 0xFFu);
+    return __half2float(*reinterpret_cast<const __half*>(&h2));
+}
+__device__ __forceinline__ uint32_t e4m3x2_of(float lo, float hi) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %2, %1;\n\tcvt.u32.u16 %0, t;\n\t}"
+        : "=r"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void rotate16_fp8(uint4& xa, uint4& yb, const float* cs, const float* sn,
+                                             const float* sx, const float* sy, const float* ix,
+                                             const float* iy) {
+    uint32_t xw[4] = {xa.x, xa.y, xa.z, xa.w}, yw[4] = {yb.x, yb.y, yb.z, yb.w};
+    #pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        uint32_t xo = 0, yo = 0;
+        #pragma unroll
+        for (int e = 0; e < 4; e += 2) {
+            float xr[2], yr[2];
+            #pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const int k = 4 * w + e + t;
+                const float x = __fmul_rn(f32_of_e4m3(xw[w] >> (8 * (e + t))), sx[k]);
+                const float y = __fmul_rn(f32_of_e4m3(yw[w] >> (8 * (e + t))), sy[k]);
+                const float xn = __fsub_rn(__fmul_rn(x, cs[k]), __fmul_rn(y, sn[k]));
+                const float yn = __fadd_rn(__fmul_rn(y, cs[k]), __fmul_rn(x, sn[k]));
+                xr[t] = __fmul_rn(xn, ix[k]);
+                yr[t] = __fmul_rn(yn, iy[k]);
+            }
+            xo |= e4m3x2_of(xr[0], xr[1]) << (8 * e);
+            yo |= e4m3x2_of(yr[0], yr[1]) << (8 * e);
+        }
+        xw[w] = xo;
+        yw[w] = yo;
+    }
+    xa = make_uint4(xw[0], xw[1], xw[2], xw[3]);
+    yb = make_uint4(yw[0], yw[1], yw[2], yw[3]);
+}
+
 // One block per (unit, page) of the call, grid-strided: the unit comes from
 // a binary search of the page offsets.  A work item is 8 frequency pairs of
-// one row: a 16-byte load from each half of the row, the rotation, two
-// 16-byte stores.
+// one row (16 for FP8 pages): a 16-byte load from each half of the row, the
+// rotation, two 16-byte stores.
+template <bool F8>
 __global__ void __launch_bounds__(256)
-k_rope(const __grid_constant__ RopeParams p, __nv_bfloat16* kpool) {
+k_rope(const __grid_constant__ RopeParams p, void* kpool_) {
     const Geo& g = p.geo;
     const int P = g.page, D = g.d, half = D / 2;
-    const int chunks = half / 8;                     // work items per row
+    constexpr int kPairs = F8 ? 16 : 8;              // frequency pairs per work item
+    const int chunks = half / kPairs;                // work items per row
     const int items = P * chunks;
     const int32_t lo = (int32_t)min64(p.pos_lo, (int64_t)INT32_MAX);
     const int32_t hi = (int32_t)min64(p.pos_hi, (int64_t)INT32_MAX);
@@ -88,14 +136,27 @@ k_rope(const __grid_constant__ RopeParams p, __nv_bfloat16* kpool) {
             const int row = w / chunks, c = w - row * chunks;
             const int32_t pos = slot_pos32(pol, idx, pg * P + row, n, held_idx, P);
             if (pos < 0 || pos < lo || pos >= hi) continue;
-            __nv_bfloat16* r = kpool + ((int64_t)phys * P + row) * D;
-            const int i0 = c * 8;
-            uint4* px = reinterpret_cast<uint4*>(r + i0);
-            uint4* py = reinterpret_cast<uint4*>(r + half + i0);
-            uint4 x = *px, y = *py;
-            rotate8(x, y, p.cs + i0, p.sn + i0);
-            *px = x;
-            *py = y;
+            const int i0 = c * kPairs;
+            if constexpr (F8) {
+                uint8_t* r = static_cast<uint8_t*>(kpool_) + ((int64_t)phys * P + row) * D;
+                uint4* px = reinterpret_cast<uint4*>(r + i0);
+                uint4* py = reinterpret_cast<uint4*>(r + half + i0);
+                uint4 x = *px, y = *py;
+                const int64_t so = ((int64_t)p.layer * g.hkv + h) * D;
+                rotate16_fp8(x, y, p.cs + i0, p.sn + i0, p.meta.kscale + so + i0,
+                             p.meta.kscale + so + half + i0, p.meta.kinv + so + i0,
+                             p.meta.kinv + so + half + i0);
+                *px = x;
+                *py = y;
+            } else {
+                __nv_bfloat16* r = static_cast<__nv_bfloat16*>(kpool_) + ((int64_t)phys * P + row) * D;
+                uint4* px = reinterpret_cast<uint4*>(r + i0);
+                uint4* py = reinterpret_cast<uint4*>(r + half + i0);
+                uint4 x = *px, y = *py;
+                rotate8(x, y, p.cs + i0, p.sn + i0);
+                *px = x;
+                *py = y;
+            }
         }
     }
 }
@@ -108,7 +169,8 @@ cudaError_t launch_rope(const sp_cache* c, const RopeParams& p, cudaStream_t s) 
     const int32_t total = p.page_off[p.n_units];
     if (total <= 0) return cudaSuccess;
     const int grid = total < 16 * c->num_sms ? total : 16 * c->num_sms;
-    k_rope<<<grid, 256, 0, s>>>(p, c->kpool);
+    if (c->geo.fp8) k_rope<true><<<grid, 256, 0, s>>>(p, c->kpool);
+    else k_rope<false><<<grid, 256, 0, s>>>(p, c->kpool);
     return cudaGetLastError();
 }
 

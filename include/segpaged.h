@@ -101,7 +101,9 @@ typedef struct sp_config {
  * f16 MMAs (see sp_set_kv_scales), prefill by turning each history tile into
  * bf16(code * scale) rows in shared memory before its bf16 MMAs (a chunk's
  * own rows enter its attention as the caller's bf16 values).
- * sp_rope_realign on FP8 pages returns SP_ERR_UNSUPPORTED. */
+ * sp_rope_realign on FP8 pages dequantises each key with its channel
+ * scales, rotates in fp32 (every product and sum rounded once) and writes
+ * the codes again as a write would. */
 typedef enum { SP_KV_BF16 = 0, SP_KV_FP8_E4M3 = 1 } sp_kv_dtype;
 
 typedef struct sp_cache sp_cache;  /* opaque host handle */
@@ -225,7 +227,10 @@ sp_status sp_set_kv_scales(sp_cache* cache, int32_t layer, const float* k_scale,
  *     k'[i + d/2] = k[i + d/2] cos a_i + k[i] sin a_i.
  * The angles are formed and reduced modulo 2 pi in double precision on the
  * host; the rotation runs in fp32 and rounds to bf16 (at most one bf16 ulp
- * from the exact rotation of the stored value).  V and the recorded positions
+ * from the exact rotation of the stored value).  FP8 pages: each code is
+ * dequantised with its channel's K scale, the pair rotated in fp32 with
+ * every product and sum rounded once, and the results written as new codes
+ * like a write (e4m3(v * fp32(1 / scale)), saturating).  V and the recorded positions
  * are not changed: a caller reusing KV computed at other positions stores it
  * at its new positions and calls this with delta = new - old.  Rows outside
  * [pos_lo, pos_hi), rows a policy does not store, and other heads are left

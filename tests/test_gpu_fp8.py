@@ -149,10 +149,8 @@ def test_append_steps_long_context():
 def test_prefill_first_chunk_then_over_fp8_history(P, n, c2):
     """A first chunk prefills over its own bf16 K/V and its write stores
     codes; the next chunk attends over the FP8 history (dequantised by the
-    oracle) plus its own bf16 rows.  RoPE realignment of FP8 pages is
-    refused and changes nothing."""
+    oracle) plus its own bf16 rows."""
     gpu_ready()
-    from head_aware_paged_gb300 import SegPagedError
     hq, hkv = 16, 4
     tot = n + c2
     cache = _mk(hq, hkv, P, 2, 2 * tot + 64, 2 * hkv * ((tot + 64) // P + 3))   # max_tokens >= both chunks
@@ -204,11 +202,6 @@ def test_prefill_first_chunk_then_over_fp8_history(P, n, c2):
         fin = np.isfinite(lref)
         assert np.array_equal(np.isfinite(lg), fin)
         assert (np.abs(lg - lref)[fin] <= bound[fin]).all(), np.abs(lg - lref)[fin].max()
-    assert cache.status() == 0
-    pool0 = cache.k_pool().clone()
-    with pytest.raises(SegPagedError):
-        cache.rope_realign(0, [0], 5)
-    assert torch.equal(cache.k_pool(), pool0)
     assert cache.status() == 0
 
 
@@ -271,3 +264,47 @@ def test_scale_and_config_validation():
         with pytest.raises(SegPagedError):
             _mk(4, hkv, 16, 1, 256, 64, **kw)
     assert c.status() == 0
+
+
+@pytest.mark.parametrize("P", [64, 16])
+def test_rope_realign_of_fp8_pages_matches_the_oracle_bit_for_bit(P):
+    """RoPE realignment of FP8 keys: every rotated code equals the oracle's
+    (dequantise with the channel scales, rotate in float32 without fused
+    operations, quantise like a write); rows outside the position range,
+    other sequences, other layers and V are untouched."""
+    gpu_ready()
+    from oracle import rope
+    hq, hkv, n = 8, 4, 700
+    cache = _mk(hq, hkv, P, 2, n + 64, 2 * 2 * hkv * (n // P + 4), layers=2)
+    pols = [W.HeadPolicy(G), W.HeadPolicy(L, 5, 70), W.HeadPolicy(G),
+            W.HeadPolicy(R, idx=np.array(sorted({3, 40, 41, 99, 250, 251, 400, 699}), np.int32))]
+    data = {}
+    for sq in range(2):
+        cache.set_policy(sq, to_c_policies([pols, pols]))
+    for l in range(2):
+        k, v = _outlier_kv(2 * n, hkv, 40 + l)
+        ks, vs = _scales(k), _scales(v)
+        cache.set_kv_scales(l, ks, vs)
+        data[l] = (ks, vs)
+        for sq in range(2):
+            cache.build(sq, l, k[sq * n:(sq + 1) * n].contiguous(), v[sq * n:(sq + 1) * n].contiguous())
+    torch.cuda.synchronize()
+    k0 = cache.k_pool().clone()
+    v0 = cache.v_pool().clone()
+    lo, hi, delta = 30, 650, 98765
+    cache.rope_realign(1, [0], delta, pos_lo=lo, pos_hi=hi)
+    torch.cuda.synchronize()
+    assert cache.status() == 0
+    assert torch.equal(cache.v_pool(), v0)
+    k1 = cache.k_pool()
+    touched = torch.zeros(k1.shape[:2], dtype=torch.bool, device="cuda")
+    ks = data[1][0]
+    for h in range(hkv):
+        sel = [(p, pg, sl) for p, pg, sl in _stored(cache, 0, 1, h) if lo <= p < hi]
+        assert sel
+        pg = torch.tensor([r[1] for r in sel], device="cuda")
+        sl = torch.tensor([r[2] for r in sel], device="cuda")
+        want = rope.realign_fp8(k0[pg, sl].cpu().numpy(), ks[h], delta)
+        np.testing.assert_array_equal(k1[pg, sl].cpu().numpy(), want)
+        touched[pg, sl] = True
+    assert torch.equal(k1[~touched], k0[~touched])
