@@ -129,14 +129,32 @@ def barrier(ws):
         dist.barrier()
 
 
+def _dist_device():
+    import torch.distributed as dist
+    return "cuda" if dist.get_backend() == "nccl" else "cpu"
+
+
 def reduce_max(x: float, ws: int) -> float:
     if ws == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=_dist_device())
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_rate(units: float, ms: float, ws: int) -> float:
+    """Whole-job rate: the units every rank processed, summed, over the
+    slowest rank's time (units per second)."""
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([units], dtype=torch.float64, device=_dist_device())
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
+        units = float(t.item())
+        ms = reduce_max(ms, ws)
+    return units / (ms / 1e3)
 
 
 # ------------------------------------------------------------ workloads
@@ -512,7 +530,7 @@ def run_ours(args, ws, rank):
     total_ms = reduce_max(float(sum(step_ms)), ws)
     assert st.cache.status() == 0
     scale = 1e-12 if not decode else 1e-9
-    value = ws * sum(work) * scale / (total_ms / 1e3)
+    value = job_rate(float(sum(work)), float(sum(step_ms)), ws) * scale
 
     # end-to-end through the same C-ABI calls with host buffers (prefill only)
     e2e = None
@@ -525,8 +543,8 @@ def run_ours(args, ws, rank):
         e0, e1 = st.run_e2e_steps(e2e_steps)
         torch.cuda.synchronize()
         assert st.cache.status() == 0
-        e2e_ms = reduce_max(e0.elapsed_time(e1), ws)
-        e2e = {"value": ws * st.work * e2e_steps * scale / (e2e_ms / 1e3), "unit": st.unit,
+        e2e = {"value": job_rate(float(st.work * e2e_steps), e0.elapsed_time(e1), ws) * scale,
+               "unit": st.unit,
                "h2d_bytes_per_step": st.h2d_bytes, "d2h_bytes_per_step": st.d2h_bytes}
     else:
         st.setup_e2e()
@@ -536,9 +554,9 @@ def run_ours(args, ws, rank):
         e0, e1, w = st.run_e2e_steps(3)
         torch.cuda.synchronize()
         assert st.cache.status() == 0
-        e2e_ms = reduce_max(e0.elapsed_time(e1), ws)
+        e2e_rate = job_rate(float(w), e0.elapsed_time(e1), ws)
         bytes_in, bytes_out = st.h2d_bytes, st.d2h_bytes
-        e2e = {"value": ws * w * scale / (e2e_ms / 1e3), "unit": st.unit,
+        e2e = {"value": e2e_rate * scale, "unit": st.unit,
                "h2d_bytes_per_step": bytes_in, "d2h_bytes_per_step": bytes_out}
 
     if rank != 0:
