@@ -642,12 +642,12 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                         resc = true;
                     }
                     const float mb = m == -INFINITY ? 0.f : m;
-                    // PV of the previous tile must be done before P is overwritten
-                    // and before O is rescaled
-                    if (k > 0) {
-                        if (!mbar_wait(&o_full[t], (k - 1) & 1, abort_flag, status)) { ok = false; break; }
-                        tc_fence_after();
-                    }
+                    // The previous tile's PV must be done before P is overwritten
+                    // and before O is rescaled.  It is: this tile's S arrived
+                    // through a tcgen05.commit issued after that PV, and a commit
+                    // tracks every earlier tcgen05 operation of the issuing
+                    // thread, so no separate wait on o_full is needed here (the
+                    // epilogue still waits for the item's last PV).
                     if (__any_sync(0xffffffffu, resc)) {
                         #pragma unroll
                         for (int ch = 0; ch < D / 16; ++ch) {
