@@ -244,8 +244,24 @@ void* stage_acquire(sp_cache* c, size_t bytes, int* slot) {
     return c->stage_buf[si];
 }
 
+namespace {
+// Staging buffer -> device memory, read by the SMs through the mapped host
+// address: no copy engine is involved, so the upload never queues behind the
+// caller's own large host<->device transfers on the copy engines.
+__global__ void k_stage_copy(const int4* __restrict__ src, int4* __restrict__ dst, size_t n) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+        dst[i] = src[i];
+}
+}  // namespace
+
 cudaError_t stage_copy(sp_cache* c, int slot, void* dst, size_t bytes, cudaStream_t s) {
-    cudaError_t e = cudaMemcpyAsync(dst, c->stage_buf[slot], bytes, cudaMemcpyHostToDevice, s);
+    if (bytes % sizeof(int4) != 0 || (reinterpret_cast<uintptr_t>(dst) & 15)) return cudaErrorInvalidValue;
+    const size_t n = bytes / sizeof(int4);
+    if (n > 0) {
+        const size_t blocks = std::min<size_t>((n + 255) / 256, (size_t)4 * c->num_sms);
+        k_stage_copy<<<(unsigned)blocks, 256, 0, s>>>(c->stage_dev[slot], static_cast<int4*>(dst), n);
+    }
+    cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess) e = cudaEventRecord(c->stage_ev[slot], s);
     return e;
 }
@@ -377,7 +393,10 @@ sp_status sp_cache_create(const sp_config* cfg, void* pool, void* meta, void* ws
                                            4 * (size_t)std::max(cfg->max_idx_per_seq, 1), 256));
     for (int i = 0; i < sp_cache::kStaging && e == cudaSuccess; ++i) {
         e = cudaHostAlloc(reinterpret_cast<void**>(&c->stage_buf[i]), c->stage_bytes,
-                          cudaHostAllocDefault);
+                          cudaHostAllocMapped);
+        void* dp = nullptr;
+        if (e == cudaSuccess) e = cudaHostGetDevicePointer(&dp, c->stage_buf[i], 0);
+        c->stage_dev[i] = static_cast<const int4*>(dp);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->stage_ev[i], cudaEventDisableTiming);
     }
     if (e != cudaSuccess) { delete c; return cuda_fail(e, "pinned staging buffers"); }

@@ -154,6 +154,7 @@ struct sp_cache {
     // a buffer is refilled only after the copy that last read it has run.
     static constexpr int kStaging = 4;
     int4* stage_buf[kStaging] = {};
+    const int4* stage_dev[kStaging] = {};        // the same buffers as device addresses (mapped)
     cudaEvent_t stage_ev[kStaging] = {};
     size_t stage_bytes = 0;                       // size of each buffer
     int stage_next = 0;
