@@ -354,26 +354,30 @@ class DecodeStep:
         return sum(self.cache.count_decode_bytes(l, self.seqs, [t] * self.B)
                    for l in range(self.layers))
 
-    # host-buffer (end-to-end) variant: each layer's q / new k / new v come
-    # from pinned host memory (one packed copy per layer) and its out / lse
-    # go back (one packed copy); uploads, kernels and downloads run on three
-    # streams, so layer l+1's upload and layer l-1's download overlap layer
-    # l's kernels
+    # host-buffer (end-to-end) variant: a step's q / new k / new v for all
+    # layers come from pinned host memory in one packed copy and its out /
+    # lse for all layers go back in one; two steps are in flight (two device
+    # buffer sets) on upload, kernel and download streams, so step i+1's
+    # upload and step i-1's download overlap step i's kernels
     def setup_e2e(self):
         import torch
         nq, nk = self.qs.numel(), self.kn.numel()
         self.e2e_split = (nq, nq + nk, nq + 2 * nk)
-        packed = torch.cat([self.qs.reshape(-1), self.kn.reshape(-1), self.vn.reshape(-1)])
-        self.h_in = packed.cpu().pin_memory()
-        self.d_in = [torch.empty_like(packed) for _ in range(self.layers)]
+        per_layer = torch.cat([self.qs.reshape(-1), self.kn.reshape(-1), self.vn.reshape(-1)])
+        self.e2e_in_words = per_layer.numel()
+        self.h_in = per_layer.repeat(self.layers).cpu().pin_memory()
         no, nl = self.out.numel(), self.lse.numel()      # out bf16, lse fp32 (2 bf16 slots each)
-        self.d_out = [torch.empty(no + 2 * nl, dtype=torch.bfloat16, device=packed.device)
-                      for _ in range(self.layers)]
-        self.h_out = [torch.empty(no + 2 * nl, dtype=torch.bfloat16).pin_memory() for _ in range(self.layers)]
+        self.e2e_out_words = no + 2 * nl
+        dev = per_layer.device
+        self.d_in = [torch.empty(self.h_in.numel(), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        self.d_out = [torch.empty(self.e2e_out_words * self.layers, dtype=torch.bfloat16, device=dev)
+                      for _ in range(2)]
+        self.h_out = [torch.empty(self.e2e_out_words * self.layers, dtype=torch.bfloat16).pin_memory()
+                      for _ in range(2)]
         self.streams = [torch.cuda.Stream() for _ in range(3)]
-        self.ev = {k: [torch.cuda.Event() for _ in range(self.layers)] for k in ("in", "done", "out")}
-        self.h2d_bytes = packed.numel() * 2 * self.layers
-        self.d2h_bytes = (no + 2 * nl) * 2 * self.layers
+        self.ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "done", "out")}
+        self.h2d_bytes = self.h_in.numel() * 2
+        self.d2h_bytes = self.h_out[0].numel() * 2
 
     def run_e2e_steps(self, n):
         """n decode steps through the C ABI with host buffers; returns (CUDA
@@ -386,32 +390,31 @@ class DecodeStep:
         for st_ in self.streams:
             st_.wait_event(start)
         a, b, e = self.e2e_split
-        no = self.out.numel()
+        no, wi, wo = self.out.numel(), self.e2e_in_words, self.e2e_out_words
         work = 0
         for step in range(n):
             work += self.step_bytes(self.t)
+            k = step % 2
+            din, dout = self.d_in[k], self.d_out[k]
+            with torch.cuda.stream(sh):
+                if step >= 2:
+                    sh.wait_event(self.ev["done"][k])        # step-2's kernels read din
+                din.copy_(self.h_in, non_blocking=True)
+                self.ev["in"][k].record(sh)
+            sc.wait_event(self.ev["in"][k])
+            if step >= 2:
+                sc.wait_event(self.ev["out"][k])            # step-2's outputs are home
             for l in range(self.layers):
-                din, dout = self.d_in[l], self.d_out[l]
-                q = din[:a].view(self.qs.shape)
-                kn = din[a:b].view(self.kn.shape)
-                vn = din[b:e].view(self.vn.shape)
-                out = dout[:no].view(self.out.shape)
-                lse = dout[no:].view(torch.float32).view(self.lse.shape)
-                with torch.cuda.stream(sh):
-                    if step > 0:
-                        sh.wait_event(self.ev["done"][l])     # last step's kernels read din
-                    din.copy_(self.h_in, non_blocking=True)
-                    self.ev["in"][l].record(sh)
-                sc.wait_event(self.ev["in"][l])
-                if step > 0:
-                    sc.wait_event(self.ev["out"][l])         # last step's outputs are home
-                self.cache.append_kv(l, self.seqs, self.cu, kn, vn, stream=sc)
-                self.cache.decode(l, self.seqs, q, out, lse, stream=sc)
-                self.ev["done"][l].record(sc)
-                sd.wait_event(self.ev["done"][l])
-                with torch.cuda.stream(sd):
-                    self.h_out[l].copy_(dout, non_blocking=True)
-                    self.ev["out"][l].record(sd)
+                li, lo_ = din[l * wi:(l + 1) * wi], dout[l * wo:(l + 1) * wo]
+                self.cache.append_kv(l, self.seqs, self.cu, li[a:b].view(self.kn.shape),
+                                     li[b:e].view(self.vn.shape), stream=sc)
+                self.cache.decode(l, self.seqs, li[:a].view(self.qs.shape), lo_[:no].view(self.out.shape),
+                                  lo_[no:].view(torch.float32).view(self.lse.shape), stream=sc)
+            self.ev["done"][k].record(sc)
+            sd.wait_event(self.ev["done"][k])
+            with torch.cuda.stream(sd):
+                self.h_out[k].copy_(dout, non_blocking=True)
+                self.ev["out"][k].record(sd)
             self.t += 1
         for st_ in self.streams:
             cur.wait_stream(st_)
