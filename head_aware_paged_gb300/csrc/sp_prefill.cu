@@ -215,7 +215,7 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
     int* status = p.meta.status;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int G = gridDim.x, cta = blockIdx.x;
+    const int cta = blockIdx.x;
     const Geo& g = p.geo;
     const int nq = p.nq;
     // the work list: in the parameters (generic loads of the parameter
@@ -616,14 +616,15 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                         for (int c = 0; c < 128; ++c)
                             sr[c] = ((vm[c >> 5] >> (c & 31)) & 1u) ? sr[c] : 0xff800000u;
                     }
-                    // row maximum (raw score units; the scale is positive)
+                    // row maximum (raw score units; the scale is positive): eight
+                    // running maxima, two new columns each per three-input max
                     float tmax;
                     {
                         float m8[8];
                         #pragma unroll
-                        for (int a = 0; a < 8; ++a) m8[a] = __uint_as_float(sr[a]);
+                        for (int a = 0; a < 8; ++a) m8[a] = fmaxf(__uint_as_float(sr[a]), __uint_as_float(sr[8 + a]));
                         #pragma unroll
-                        for (int e = 8; e < 128; e += 16)
+                        for (int e = 16; e < 128; e += 16)
                             #pragma unroll
                             for (int a = 0; a < 8; ++a)
                                 m8[a] = fmax3(m8[a], __uint_as_float(sr[e + a]), __uint_as_float(sr[e + 8 + a]));
