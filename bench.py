@@ -632,19 +632,30 @@ def cpu_baseline(st, wl, decode, target_s=12.0):
         pt = [(p.kind, p.sink, p.window, None) for p in st.pols[0]]
         qf = st.qs.float().cpu().numpy()
         t = st.n - 1
+        k0 = v0 = None
         for b in seqs:
             k = W.normal((st.n, wl.hkv, wl.d), W.tensor_seed(0, "k", b, 0)).float().numpy()
             v = W.normal((st.n, wl.hkv, wl.d), W.tensor_seed(0, "v", b, 0)).float().numpy()
+            if b == 0:
+                k0, v0 = k, v
             t1 = time.perf_counter()
             oracle.attend(qf[b:b + 1], k, v, [t], pt, "f32", threads=threads)
             busy += time.perf_counter() - t1
             nbytes += st.cache.count_decode_bytes(0, [b], [t])
+        # the same query of sequence 0 on one thread
+        t1 = time.perf_counter()
+        oracle.attend(qf[0:1], k0, v0, [t], pt, "f32", threads=1)
+        one = {"value": st.cache.count_decode_bytes(0, [0], [t]) / (time.perf_counter() - t1) / 1e9,
+               "cores": 1, "sample": "layer 0, sequence 0, one decode query"}
         return {"value": nbytes / busy / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
                 "sample": "layer 0, sequences 0 and %d, one decode query each over %d cached "
-                          "tokens (fp32 C oracle)" % (wl.seqs - 1, st.n)}
+                          "tokens (fp32 C oracle)" % (wl.seqs - 1, st.n), "one_thread": one}
     (dt, fl, n), *_ = st.oracle_sample(W.policies(wl)[0], target_s, threads)
+    (dt1, fl1, n1), *_ = st.oracle_sample(W.policies(wl)[0], target_s / threads, 1)
     return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": "%d of %d query rows (all %d heads), fp32 C oracle" % (n, st.L, wl.hq)}
+            "sample": "%d of %d query rows (all %d heads), fp32 C oracle" % (n, st.L, wl.hq),
+            "one_thread": {"value": fl1 / dt1 / 1e12, "cores": 1,
+                           "sample": "%d of %d query rows (all %d heads)" % (n1, st.L, wl.hq)}}
 
 
 def run_reference(args, ws, rank):
