@@ -77,7 +77,11 @@ def _rand_policies(hkv, max_len, rng, sink_hi=9, win_hi=700, idx_hi=500):
 
 
 @pytest.mark.parametrize("P,d,hq,hkv", [(64, 128, 16, 4), (16, 64, 8, 4), (128, 128, 12, 3),
-                                        (32, 64, 6, 3)])
+                                        (32, 64, 6, 3),
+                                        # odd GQA groups (one query tile per item) and the
+                                        # remaining (head_dim, page size) kernel instances
+                                        (16, 128, 6, 2), (32, 128, 8, 8), (64, 64, 4, 2),
+                                        (128, 64, 9, 3)])
 def test_chunked_ragged_prefill_with_history(P, d, hq, hkv):
     """Several sequences prefilled in ragged chunks (history from pages, the
     rest from the chunk), mixed classes incl. RETRIEVAL, then decode; every
