@@ -951,7 +951,9 @@ def run_op_select(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default 20; the decode workload 64, the step count of "
+                         "its configuration)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="mistral7b_prefill_8k",
@@ -964,6 +966,9 @@ def main():
     ap.add_argument("--op", default="", choices=["", "rope_realign", "pack", "select", "chunk_prefill"],
                     help="time one library operation instead of the attention step")
     args = ap.parse_args()
+    if args.steps is None:
+        args.steps = 64 if (args.workload == "llama3_8b_decode_32k" and not args.op
+                            and args.impl == "ours") else 20
     if args.warmup < 3:
         args.warmup = 3
     if args.op:
