@@ -19,6 +19,10 @@
 //         slot rule); "ERR" on an empty or duplicated slot.
 // mode 2  slot table of a unit holding n tokens: "S pages" then one line
 //         "P pos..." per page (-1 = empty slot).
+// mode 3  the writes of i_lo chunks (sizes follow the index list) applied
+//         one after another as the scatter kernel applies them (kept tokens
+//         from retained_items, slots from unit_slot): after each chunk the
+//         table in mode 2's format; "ERR" on a slot outside the unit's pages.
 #include <algorithm>
 #include <cstdio>
 #include <vector>
@@ -131,6 +135,35 @@ static void slot_case(const UnitPol& u, const int32_t* idx, int P, int64_t n) {
     }
 }
 
+static void write_case(const UnitPol& u, const int32_t* idx, int P, const std::vector<int64_t>& chunks) {
+    std::vector<int64_t> table;
+    int64_t n = 0;
+    for (int64_t c : chunks) {
+        const int64_t n_new = n + c;
+        const int64_t pages = unit_pages(u, idx, n_new, P);
+        table.resize(pages * P, -1);
+        const ItemRanges r = retained_items(u, idx, n, n_new, P);
+        for (int k = 0; k < 2; ++k)
+            for (int64_t it = r.lo[k]; it < r.hi[k]; ++it) {
+                const int64_t pos = u.kind == kRetrieval ? idx[it] : it;
+                const int64_t us = unit_slot(u, idx, pos, P);
+                if (us < 0 || us >= pages * P) {
+                    printf("ERR token %lld to slot %lld of %lld\n", (long long)pos, (long long)us,
+                           (long long)(pages * P));
+                    continue;
+                }
+                table[us] = pos;
+            }
+        n = n_new;
+        printf("S %lld\n", (long long)pages);
+        for (int64_t pg = 0; pg < pages; ++pg) {
+            printf("P");
+            for (int sl = 0; sl < P; ++sl) printf(" %lld", (long long)table[pg * P + sl]);
+            printf("\n");
+        }
+    }
+}
+
 int main() {
     int cases = 0;
     if (scanf("%d", &cases) != 1) return 2;
@@ -143,9 +176,17 @@ int main() {
         std::vector<int32_t> idx(n_idx > 0 ? n_idx : 1, 0);
         for (int j = 0; j < n_idx; ++j)
             if (scanf("%d", &idx[j]) != 1) return 2;
+        std::vector<int64_t> chunks;
+        if (mode == 3)
+            for (long long j = 0; j < i_lo; ++j) {
+                long long c;
+                if (scanf("%lld", &c) != 1) return 2;
+                chunks.push_back(c);
+            }
         const UnitPol u = make_pol(kind, sink, window, P, n_idx);
         printf("C %d\n", k);
-        if (mode == 0) prefill_case(u, idx.data(), P, n, i_lo, i_hi);
+        if (mode == 3) write_case(u, idx.data(), P, chunks);
+        else if (mode == 0) prefill_case(u, idx.data(), P, n, i_lo, i_hi);
         else if (mode == 1) decode_case(u, idx.data(), P, n, i_lo);
         else slot_case(u, idx.data(), P, n);
     }

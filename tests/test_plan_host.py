@@ -12,7 +12,8 @@ ranges this test checks, bit for bit:
     pages (section 3: per-head page lists);
   * decode: the slot ranges one query reads hold exactly V(t);
   * storage: the position held by every slot of a unit equals the oracle's
-    page model of the same write rule.
+    page model of the same write rule, both from the closed-form slot rule
+    and after the scatter kernels' per-write rule applied chunk by chunk.
 """
 import os
 import shutil
@@ -43,8 +44,10 @@ def harness(tmp_path_factory):
 def _run(exe, cases):
     lines = [str(len(cases))]
     for c in cases:
-        mode, kind, sink, window, P, n, i_lo, i_hi, idx = c
-        lines.append(" ".join(str(x) for x in [mode, kind, sink, window, P, n, i_lo, i_hi, len(idx)] + list(idx)))
+        mode, kind, sink, window, P, n, i_lo, i_hi, idx = c[:9]
+        extra = list(c[9]) if len(c) > 9 else []
+        lines.append(" ".join(str(x) for x in [mode, kind, sink, window, P, n, i_lo, i_hi, len(idx)]
+                              + list(idx) + extra))
     out = subprocess.run([exe], input="\n".join(lines) + "\n", capture_output=True, text=True, check=True).stdout
     res, cur = [], None
     for ln in out.splitlines():
@@ -62,8 +65,10 @@ def _run(exe, cases):
             cur["D"] = tuple(int(x) for x in f[1:])
         elif f[0] == "S":
             cur["S"] = int(f[1])
+            cur.setdefault("tables", []).append([])
         elif f[0] == "P":
             cur["P"].append([int(x) for x in f[1:]])
+            cur["tables"][-1].append([int(x) for x in f[1:]])
     assert len(res) == len(cases)
     return res
 
@@ -149,3 +154,27 @@ def test_slot_tables_match_the_page_model(harness):
         want = pagemodel.stored_positions(kind, sink, window, idx if kind == R else None, n, P)
         assert r["S"] == len(want), c[:6]
         assert r["P"] == want, c[:6]
+
+
+def test_chunked_writes_leave_the_page_model_state(harness):
+    """The scatter kernels' write rule (kept tokens per write, the slot of
+    each) applied chunk by chunk leaves after every chunk exactly the slot
+    contents of the oracle's token-by-token page model."""
+    rng = np.random.default_rng(14)
+    cases = []
+    for _ in range(150):
+        P = int(rng.choice([16, 32, 64, 128]))
+        m = int(rng.integers(1, 6))
+        chunks = [int(x) for x in rng.choice([1, 2, 15, 16, 17, 64, 100, 333, 1000], size=m)]
+        kind, sink, window, idx = _policy(rng, sum(chunks) + 30)
+        cases.append((3, kind, sink, window, P, sum(chunks), m, 0, idx, chunks))
+    res = _run(harness, cases)
+    for c, r in zip(cases, res):
+        _, kind, sink, window, P, _, m, _, idx, chunks = c
+        assert not r["ERR"], (c[:8], r["ERR"][:3])
+        assert len(r["tables"]) == m
+        n = 0
+        for ch, got in zip(chunks, r["tables"]):
+            n += ch
+            want = pagemodel.stored_positions(kind, sink, window, idx if kind == R else None, n, P)
+            assert got == want, (c[:8], n)
