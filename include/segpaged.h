@@ -184,10 +184,11 @@ sp_status sp_attention_decode(sp_cache* cache, int32_t layer,
  * computation as sp_attention_decode, but the split-KV scratch (partial
  * outputs, their max / sum and the merge tickets) lives in a fixed 4 MiB
  * device array compiled into this library instead of the cache's workspace.
- * (The paper has no counterpart; this entry point is for callers that cannot
- * allocate device memory when they decode: a plain C host without a device
- * allocator, or a serving loop that must not call cudaMalloc mid-step because
- * it can synchronise the device or is forbidden after start-up.)
+ * (The method's sources have no counterpart; this entry point is for
+ * callers that cannot allocate device memory when they decode: a plain C host
+ * without a device allocator, or a serving loop that must not call cudaMalloc
+ * mid-step because it can synchronise the device or is forbidden after
+ * start-up.)
  *   - The caller still passes the cache, q, out and lse, as for
  *     sp_attention_decode.
  *   - Limit: (n_seqs * num_kv_heads + SM count) * group * (head_dim + 2) * 4
@@ -235,8 +236,8 @@ sp_status sp_set_kv_scales(sp_cache* cache, int32_t layer, const float* k_scale,
  * at its new positions and calls this with delta = new - old.  Rows outside
  * [pos_lo, pos_hi), rows a policy does not store, and other heads are left
  * untouched.  SP_ERR_INVALID_ARG for a bad list or head, pos_lo > pos_hi,
- * rope_theta <= 0 or |delta| > 2^40.  The paper has no such entry point by
- * name; this is its RoPE-alignment step applied to the paged layout. */
+ * rope_theta <= 0 or |delta| > 2^40.  The news summary names no such entry
+ * point; this is its RoPE-alignment step applied to the paged layout. */
 sp_status sp_rope_realign(sp_cache* cache, int32_t layer, const int32_t* seq_ids,
                           int32_t n_seqs, int32_t kv_head, int64_t pos_lo,
                           int64_t pos_hi, int64_t delta, double rope_theta,
@@ -260,8 +261,8 @@ sp_status sp_rope_realign(sp_cache* cache, int32_t layer, const int32_t* seq_ids
  * min(topk, n - recent) + min(recent, n) indices followed by -1; counts
  * [num_kv_heads] int32 (nullable); scores [num_kv_heads][n] fp32 (nullable).
  * workspace: device scratch of sp_select_workspace_bytes(...) bytes, 256-byte
- * aligned.  Asynchronous on `stream`.  The paper has no entry point by this
- * name; it is the selection step its retrieval heads assume. */
+ * aligned.  Asynchronous on `stream`.  The runtime article names no such
+ * entry point; it is the selection step its retrieval heads assume. */
 sp_status sp_select_workspace_bytes(int32_t n_obs, int32_t n, int32_t num_q_heads,
                                     int32_t num_kv_heads, size_t* bytes);
 sp_status sp_select_heavy_hitters(const void* q_obs, int32_t n_obs, const void* k, int32_t n,
@@ -272,8 +273,8 @@ sp_status sp_select_heavy_hitters(const void* q_obs, int32_t n_obs, const void* 
 
 /* Pack / unpack one sequence for a prefill/decode-disaggregated transfer (news
  * summary, "system gains": in the PD-separated setting only the tokens each
- * head keeps travel, up to 6.3x fewer KV bytes).  The paper has no entry
- * points by these names; these carry its trimmed per-head layout across.
+ * head keeps travel, up to 6.3x fewer KV bytes).  The summary names no such
+ * entry points; these carry its trimmed per-head layout across.
  *
  * sp_pack_seq writes into the device buffer dst (256-byte aligned) a header
  * (layer count, KV heads, head_dim, page_size, tokens per layer, every unit's
