@@ -252,7 +252,9 @@ def sp_get_status(handle, stream=None) -> int:
 
 def sp_selftest_bounded_wait(handle, limit_cycles: int, mode: int, stream=None) -> None:
     """Launch the bounded-wait self-test (mode 0: the wait gives up and the
-    next status read reports SP_ERR_TIMEOUT; mode 1: the wait completes)."""
+    next status read reports SP_ERR_TIMEOUT; mode 1: the wait completes;
+    mode 2: two warps, one wait completes and one gives up, both leave
+    together and the status reports SP_ERR_TIMEOUT)."""
     check(load().sp_selftest_bounded_wait(handle, limit_cycles, mode, _stream(stream)))
 
 

@@ -110,7 +110,6 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 }
 
 bool valid_seq(const sp_cache* c, int32_t seq) { return seq >= 0 && seq < c->cfg.max_seqs; }
-bool valid_layer(const sp_cache* c, int32_t l) { return l >= 0 && l < c->cfg.num_layers; }
 
 size_t unit_index(const sp_cache* c, int seq, int layer, int h) {
     return ((size_t)seq * c->cfg.num_layers + layer) * c->cfg.num_kv_heads + h;
@@ -188,20 +187,6 @@ sp_status write_tokens(sp_cache* c, int32_t layer, const int32_t* seqs, int32_t 
     return SP_OK;
 }
 
-sp_status check_seq_list(const sp_cache* c, const int32_t* seq_ids, int32_t n_seqs) {
-    if (!seq_ids || n_seqs < 1) return fail(SP_ERR_INVALID_ARG, "empty sequence list");
-    if (n_seqs > c->cfg.max_batch) return fail(SP_ERR_INVALID_ARG, "more sequences than max_batch");
-    std::vector<uint8_t> seen(c->cfg.max_seqs, 0);
-    for (int b = 0; b < n_seqs; ++b) {
-        const int s = seq_ids[b];
-        if (!valid_seq(c, s)) return fail(SP_ERR_INVALID_ARG, "sequence id out of range");
-        if (seen[s]) return fail(SP_ERR_INVALID_ARG, "sequence listed twice");
-        if (!c->h_policy_set[s]) return fail(SP_ERR_INVALID_ARG, "sequence has no policy");
-        seen[s] = 1;
-    }
-    return SP_OK;
-}
-
 // Rows a unit holding n tokens keeps (the retained set of the slot rules):
 // GLOBAL every token, LOCAL the sink and the newest ring's worth, RETRIEVAL
 // its listed positions below n.
@@ -234,6 +219,26 @@ UnitPol encode_unit(int64_t kind, int64_t sink, int64_t window, int32_t idx_off,
 size_t align_to(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace
+
+bool valid_layer(const sp_cache* c, int32_t l) { return l >= 0 && l < c->cfg.num_layers; }
+
+sp_status check_seq_list(const sp_cache* c, const int32_t* seq_ids, int32_t n_seqs) {
+    if (!seq_ids || n_seqs < 1) return fail(SP_ERR_INVALID_ARG, "empty sequence list");
+    if (n_seqs > c->cfg.max_batch) return fail(SP_ERR_INVALID_ARG, "more sequences than max_batch");
+    // duplicates through a sorted copy on the stack (n_seqs <= max_batch <=
+    // kMaxCallSeqs): the check allocates nothing
+    int32_t sorted[kMaxCallSeqs];
+    for (int b = 0; b < n_seqs; ++b) {
+        const int s = seq_ids[b];
+        if (!valid_seq(c, s)) return fail(SP_ERR_INVALID_ARG, "sequence id out of range");
+        if (!c->h_policy_set[s]) return fail(SP_ERR_INVALID_ARG, "sequence has no policy");
+        sorted[b] = s;
+    }
+    std::sort(sorted, sorted + n_seqs);
+    for (int b = 1; b < n_seqs; ++b)
+        if (sorted[b] == sorted[b - 1]) return fail(SP_ERR_INVALID_ARG, "sequence listed twice");
+    return SP_OK;
+}
 
 void* stage_acquire(sp_cache* c, size_t bytes, int* slot) {
     if (bytes > c->stage_bytes) return nullptr;

@@ -50,21 +50,15 @@ extern "C" sp_status sp_attention_decode_static_scratch(sp_cache* c, int32_t lay
                                                        const int32_t* seq_ids, int32_t n_seqs,
                                                        const void* q, void* out, float* lse,
                                                        void* stream) {
-    if (!c || !q || !out || !seq_ids) return fail(SP_ERR_INVALID_ARG, "null argument");
-    if (layer < 0 || layer >= c->cfg.num_layers) return fail(SP_ERR_INVALID_ARG, "layer out of range");
-    if (n_seqs < 1 || n_seqs > c->cfg.max_batch)
-        return fail(SP_ERR_INVALID_ARG, "n_seqs must be in [1, max_batch]");
+    if (!c || !q || !out) return fail(SP_ERR_INVALID_ARG, "null argument");
+    if (!valid_layer(c, layer)) return fail(SP_ERR_INVALID_ARG, "layer out of range");
+    sp_status s = check_seq_list(c, seq_ids, n_seqs);
+    if (s != SP_OK) return s;
     if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 3)
         return fail(SP_ERR_INVALID_ARG, "q and out must be 4-byte aligned");
-    for (int b = 0; b < n_seqs; ++b) {
-        const int s = seq_ids[b];
-        if (s < 0 || s >= c->cfg.max_seqs) return fail(SP_ERR_INVALID_ARG, "sequence id out of range");
-        if (!c->h_policy_set[s]) return fail(SP_ERR_INVALID_ARG, "sequence has no policy");
-        for (int b2 = 0; b2 < b; ++b2)
-            if (seq_ids[b2] == s) return fail(SP_ERR_INVALID_ARG, "sequence listed twice");
-        if (c->h_seqlen[(size_t)s * c->cfg.num_layers + layer] < 1)
+    for (int b = 0; b < n_seqs; ++b)
+        if (c->h_seqlen[(size_t)seq_ids[b] * c->cfg.num_layers + layer] < 1)
             return fail(SP_ERR_INVALID_ARG, "decode needs the query's own token appended first");
-    }
     const int hkv = c->cfg.num_kv_heads, group = c->geo.group, d = c->cfg.head_dim;
     const int64_t n_units = (int64_t)n_seqs * hkv;
     // scratch layout: partial outputs, partial (m, l), tickets -- sized for the

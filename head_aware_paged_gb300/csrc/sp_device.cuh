@@ -68,6 +68,21 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     }
 }
 
+// Named barrier `kId` over `nthreads` threads (whole warps) that also ORs a
+// predicate: every participant gets true when any of them passed true.  A
+// named barrier has no time limit, so warps that must leave a loop together
+// after a bounded wait meet here right after that wait (every path reaches
+// this point) and then all leave or all stay; a later plain barrier of the
+// same warps is then met by all of them too.
+template <int kId>
+__device__ __forceinline__ bool meet_any(uint32_t nthreads, bool pred) {
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
+                 "bar.red.or.pred po, %2, %3, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+                 : "=r"(r) : "r"((uint32_t)pred), "n"(kId), "r"(nthreads) : "memory");
+    return r != 0;
+}
+
 // 2D tiled TMA load of a box at (x = inner element index, y = row) into smem,
 // completing on `bar`.  x * element size must be a multiple of 16 bytes.
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map,

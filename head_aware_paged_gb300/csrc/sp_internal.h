@@ -170,6 +170,12 @@ namespace sp {
 void* stage_acquire(sp_cache* c, size_t bytes, int* slot);
 cudaError_t stage_copy(sp_cache* c, int slot, void* dst, size_t bytes, cudaStream_t s);
 
+// Argument checks shared by the entry points (sp_api.cu); they allocate
+// nothing.  check_seq_list: 1..max_batch ids, each in range, with a policy,
+// none listed twice.
+bool valid_layer(const sp_cache* c, int32_t layer);
+sp_status check_seq_list(const sp_cache* c, const int32_t* seq_ids, int32_t n_seqs);
+
 // Error plumbing (sp_api.cu).
 sp_status fail(sp_status s, const std::string& msg);
 sp_status cuda_fail(cudaError_t e, const char* what);

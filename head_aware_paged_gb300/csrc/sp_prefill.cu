@@ -492,7 +492,12 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
         uint32_t fj = 0;
         while (true) {
             const uint32_t f = fj & 1;
-            if (!mbar_wait(&f_full[f], (fj >> 1) & 1, abort_flag, status)) break;
+            const bool got = mbar_wait(&f_full[f], (fj >> 1) & 1, abort_flag, status);
+            // The two warps decide together: either wait may give up on its
+            // own (its time limit, or the abort flag raised by another role
+            // while the codes land), and the barrier after the conversion
+            // must be met by both.  So both leave if either gave up.
+            if (meet_any<3>(64, !got)) break;
             const int4 jb = jobs[f];
             if (jb.x < 0) break;
             const float* scp = (jb.y ? p.meta.vscale : p.meta.kscale) +

@@ -346,7 +346,11 @@ sp_status sp_get_status(sp_cache* cache, void* stream, int32_t* word);
  * ([1000, 2e9] clock cycles).  mode 0: nothing arrives, the wait gives up and
  * raises the timeout flag of the cache's status word, so the next
  * sp_get_status returns SP_ERR_TIMEOUT (and clears it); mode 1: a second
- * warp arrives after limit_cycles / 8 and the status stays clear.
+ * warp arrives after limit_cycles / 8 and the status stays clear; mode 2:
+ * two warps that must leave together (the pattern of the prefill's FP8
+ * converter pair) each wait on their own barrier, one completes and one
+ * never does; both leave after the limit (SP_ERR_TIMEOUT as in mode 0) and
+ * neither is left at a named barrier.
  * Asynchronous on `stream`; SP_ERR_INVALID_ARG for other arguments. */
 sp_status sp_selftest_bounded_wait(sp_cache* cache, int64_t limit_cycles, int32_t mode,
                                    void* stream);

@@ -34,6 +34,14 @@ def test_bounded_wait_times_out_and_the_context_recovers():
         cache.status()
     assert time.time() - t0 < 10
     assert cache.status() == 0                 # the read cleared the flag
+    # two warps that must leave together, one of whose waits never completes
+    # (the FP8 converter pair's pattern): both leave, the kernel returns
+    t0 = time.time()
+    sp_selftest_bounded_wait(cache.handle, 2_000_000, 2)
+    with pytest.raises(SegPagedError, match="SP_ERR_TIMEOUT"):
+        cache.status()
+    assert time.time() - t0 < 10
+    assert cache.status() == 0
     # the same context still computes attention correctly
     k = W.normal((n, 2, d), 1, device="cuda")
     v = W.normal((n, 2, d), 2, device="cuda")
@@ -45,7 +53,7 @@ def test_bounded_wait_times_out_and_the_context_recovers():
     compare(out, ref, lse, lref, "decode after a timed-out wait")
     assert cache.status() == 0
     # arguments outside the documented range are refused before any launch
-    for limit, mode in ((10, 0), (2_000_000, 2), (3_000_000_000, 0)):
+    for limit, mode in ((10, 0), (2_000_000, 3), (2_000_000, -1), (3_000_000_000, 0)):
         with pytest.raises(SegPagedError):
             sp_selftest_bounded_wait(cache.handle, limit, mode)
     assert cache.status() == 0
