@@ -1,19 +1,25 @@
 """Benchmark of the head-aware paged attention hot path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload mistral7b_prefill_8k|llama3_8b_decode_32k|llama33_70b_prefill_128k]
+                    [--workload llama33_70b_prefill_128k|mistral7b_prefill_8k|llama3_8b_decode_32k]
 
-Prints ONE JSON line (rank 0).  Default workload: the Mistral-7B-shaped
-prefill layer (Hq 32 / Hkv 8, d 128, one sequence of 8192 tokens, page 64,
-1 GLOBAL + 7 LOCAL(4, 1024) KV heads).  One step is one pass of the whole
-path over that batch: causal prefill of the 8192-token chunk, the trimmed
-KV write of the chunk (page allocation + scatter), one decode token
-(append + split-KV decode), and the release of the sequence's pages.  The
-head-class policy is set once, offline, before timing.
+Prints ONE JSON line (rank 0).  Default workload: the Llama-3.3-70B-shaped
+long prefill, every one of its 64 layers (Hq 64 / Hkv 8, d 128, one
+sequence of 131,072 tokens, page 64; 77 of the 512 (layer, KV head) units
+GLOBAL by seed, the rest LOCAL(4, 8192)), each layer with its own policy
+row and its own Q/K/V resident in HBM.  One step is one pass of the whole
+path over that sequence: per layer the causal prefill of all 131,072 rows
+and the trimmed KV write of the chunk (page allocation + scatter), then one
+decode token per layer (append + split-KV decode), then the release of the
+sequence's pages.  The head-class policy is set once, offline, before
+timing.  The same line carries, under "decode", the Llama-3-8B-shaped
+decode batch (32 layers, 32 sequences x 32,768 cached tokens, 64 steps).
 
 Metric: visible-pair TFLOP/s (FLOP = 4 d per visible (query, key) pair, for
-the prefill rows and the decode row) for prefill workloads; visible-KV GB/s
+the prefill rows and the decode rows) for prefill workloads; visible-KV GB/s
 (2 d bytes of K and V per visible key and head) for the decode workload.
+The roofline of each record is its dominant kernel over all of its launches
+in the timed steps (CUDA events around each launch on the launching stream).
 Timing: CUDA events on the launching stream after W warm-up steps; L2 is
 flushed (256 MB write) between steps, outside the timed events.  With
 --gpus N > 1 (torchrun), every rank runs the same workload on its own GPU
@@ -21,7 +27,7 @@ flushed (256 MB write) between steps, outside the timed events.  With
 the ranks' work over the slowest rank's time.
 
 --impl reference times the CPU oracle (plain fp32 C, all host cores) on a
-bounded sample of the same workload, in the same units.
+bounded sample of the same workload, in the same units, with the same config.
 """
 from __future__ import annotations
 
@@ -159,74 +165,125 @@ def job_rate(units: float, ms: float, ws: int) -> float:
 
 # ------------------------------------------------------------ workloads
 
-class PrefillStep:
-    """Prefill + trimmed KV write + one decode token + release, one sequence."""
+def unit_pages(p, n: int, P: int) -> int:
+    """Pages one (sequence, layer, KV head) unit holds after n tokens (pool
+    sizing only: GLOBAL ceil(n/P); LOCAL its sink pages plus at most its ring
+    of ceil(W/P) + 1 pages; RETRIEVAL its listed positions below n)."""
+    if p.kind == W.GLOBAL:
+        return -(-n // P)
+    if p.kind == W.LOCAL:
+        ring = -(-p.window // P) + 1
+        return -(-min(n, p.sink) // P) + min(ring, -(-max(0, n - p.sink) // P))
+    return -(-int((np.asarray(p.idx) < n).sum()) // P)
 
-    def __init__(self, wl, layer_policies, device="cuda"):
+
+class PrefillStep:
+    """One sequence, every layer of the workload: per layer the causal
+    prefill of the whole sequence as one chunk and the trimmed KV write of
+    that chunk (page allocation + scatter); then one decode token in every
+    layer (append + split-KV decode); then the release of the sequence's
+    pages.  Each layer has its own head-class row and its own Q/K/V, all
+    resident in HBM before timing; the policy is set once, offline."""
+
+    def __init__(self, wl, device="cuda"):
         import torch
         from head_aware_paged_gb300 import Config, Policy, SegPagedCache
         self.wl = wl
         L = wl.seq_len
         self.L = L
-        pol = [[Policy(p.kind, p.sink, p.window, None if p.idx is None else p.idx.tolist())
-                for p in layer_policies]]
-        pages = 0
-        for p in layer_policies:
-            pages += (L + 1 + wl.page - 1) // wl.page + 2
-        self.cfg = Config(num_layers=1, num_q_heads=wl.hq, num_kv_heads=wl.hkv, head_dim=wl.d,
-                          page_size=wl.page, max_seqs=2, max_seq_len=L + 64, num_pages=2 * pages,
-                          max_idx_per_seq=max(1, sum(0 if p.idx is None else len(p.idx)
-                                                     for p in layer_policies)),
-                          max_tokens=L, max_batch=1)
+        self.layers = wl.layers
+        self.pols = W.policies(wl)
+        pages = sum(unit_pages(p, L + 1, wl.page) for row in self.pols for p in row)
+        n_idx = sum(0 if p.idx is None else len(p.idx) for row in self.pols for p in row)
+        self.cfg = Config(num_layers=self.layers, num_q_heads=wl.hq, num_kv_heads=wl.hkv,
+                          head_dim=wl.d, page_size=wl.page, max_seqs=1, max_seq_len=L + 64,
+                          num_pages=pages + 64, max_idx_per_seq=max(1, n_idx), max_tokens=L,
+                          max_batch=1)
         self.cache = SegPagedCache(self.cfg)
-        self.cache.set_policy(0, pol)
-        self.cache.set_policy(1, pol)            # the second request slot of the e2e leg
-        self.q, self.k, self.v = W.qkv(wl, L + 1, 0, 0, device=device)
-        self.q1 = self.q[L:].contiguous()
-        self.k1 = self.k[L:].contiguous()
-        self.v1 = self.v[L:].contiguous()
-        self.q, self.k, self.v = (self.q[:L].contiguous(), self.k[:L].contiguous(),
-                                  self.v[:L].contiguous())
-        self.out = torch.empty_like(self.q)
+        self.cache.set_policy(0, [[Policy(p.kind, p.sink, p.window,
+                                          None if p.idx is None else p.idx.tolist())
+                                   for p in row] for row in self.pols])
+        # per layer: rows 0..L-1 are the prefill chunk, row L the decode token
+        self.q, self.k, self.v, self.q1, self.k1, self.v1 = [], [], [], [], [], []
+        for l in range(self.layers):
+            q, k, v = W.qkv(wl, L + 1, 0, l, device=device)
+            for lst, t in ((self.q, q), (self.k, k), (self.v, v)):
+                lst.append(t[:L])
+            for lst, t in ((self.q1, q), (self.k1, k), (self.v1, v)):
+                lst.append(t[L:])
+            del q, k, v
+        self.out = torch.empty_like(self.q[0])
         self.lse = torch.empty(L, wl.hq, dtype=torch.float32, device=device)
-        self.out1 = torch.empty_like(self.q1)
+        self.out1 = torch.empty_like(self.q1[0])
         self.lse1 = torch.empty(1, wl.hq, dtype=torch.float32, device=device)
-        pairs = self.cache.count_prefill_pairs(0, 0, 0, L)
-        dec_pairs = self.cache.count_decode_bytes(0, [0], [L]) // (2 * wl.d * 2) * (wl.hq // wl.hkv)
-        self.prefill_flop = 4 * wl.d * pairs
-        self.work = 4 * wl.d * (pairs + dec_pairs)      # FLOP per step
-        self.kernels_per_step = 7                        # prefill, 2x(alloc+scatter), decode, release
+        grp = wl.hq // wl.hkv
+        self.pf_flop = [4 * wl.d * self.cache.count_prefill_pairs(0, l, 0, L)
+                        for l in range(self.layers)]
+        dec_pairs = sum(self.cache.count_decode_bytes(l, [0], [L]) // (2 * wl.d * 2) * grp
+                        for l in range(self.layers))
+        self.prefill_flop = sum(self.pf_flop)
+        self.work = self.prefill_flop + 4 * wl.d * dec_pairs      # FLOP per step
+        # launches per step: per layer the prefill (plus the copy kernel of a
+        # work list too large for the kernel parameters) and the chunk's
+        # append (allocator + scatter); per layer the decode token's append
+        # and decode; one release
+        pairs = grp // 2 if grp % 2 == 0 else grp
+        items = wl.hkv * (-(-L // 128)) * pairs
+        words = items + (min(items, 152) + 1 + 3) // 4
+        pf_launches = 1 + (0 if words <= 1344 else 1)
+        self.kernels_per_step = self.layers * (pf_launches + 2) + self.layers * 3 + 1
         self.unit = "TFLOP/s"
 
     def run(self, ev_pf=None):
+        """One step; ev_pf (optional): a (start, end) event pair per layer
+        recorded around that layer's prefill launch."""
         c = self.cache
-        if ev_pf is not None:
-            ev_pf[0].record()
-        c.prefill(0, [0], [0, self.L], self.q, self.k, self.v, self.out, self.lse)
-        if ev_pf is not None:
-            ev_pf[1].record()
-        c.append_kv(0, [0], [0, self.L], self.k, self.v)
-        c.append_kv(0, [0], [0, 1], self.k1, self.v1)
-        c.decode(0, [0], self.q1, self.out1, self.lse1)
+        for l in range(self.layers):
+            if ev_pf is not None:
+                ev_pf[l][0].record()
+            c.prefill(l, [0], [0, self.L], self.q[l], self.k[l], self.v[l], self.out, self.lse)
+            if ev_pf is not None:
+                ev_pf[l][1].record()
+            c.append_kv(l, [0], [0, self.L], self.k[l], self.v[l])
+        for l in range(self.layers):
+            c.append_kv(l, [0], [0, 1], self.k1[l], self.v1[l])
+            c.decode(l, [0], self.q1[l], self.out1, self.lse1)
         c.release(0)
 
-    # host-buffer (end-to-end) variant: every step uploads its q/k/v from
-    # pinned host memory and reads out/lse back; consecutive steps run as two
-    # requests in flight (sequence slots 0 and 1, two device buffer sets), so
-    # step i+1's upload and step i-1's download overlap step i's kernels
+    # host-buffer (end-to-end) variant: every layer's q/k/v chunk is uploaded
+    # from pinned host memory and its out/lse read back; the decode tokens of
+    # all layers go up in one packed copy and their outputs come back in one.
+    # Layers alternate between two device buffer sets and run on upload,
+    # kernel and download streams, so layer l+1's upload and layer l-1's
+    # download overlap layer l's kernels.  One pinned host set of chunk
+    # inputs (layer 0's values) is uploaded for every layer: the bytes moved
+    # are those of a real pass, only the values repeat.
     def setup_e2e(self):
         import torch
         pin = lambda t: t.cpu().pin_memory()
-        self.h_in = [pin(t) for t in (self.q, self.k, self.v, self.q1, self.k1, self.v1)]
-        self.dev = [[torch.empty_like(t) for t in (self.q, self.k, self.v, self.q1, self.k1, self.v1,
-                                                    self.out, self.lse, self.out1, self.lse1)]
-                    for _ in range(2)]
-        self.h_out = [[torch.empty(t.shape, dtype=t.dtype).pin_memory()
-                       for t in (self.out, self.lse, self.out1, self.lse1)] for _ in range(2)]
+        self.h_in = [pin(t) for t in (self.q[0], self.k[0], self.v[0])]
+        self.dset = [[torch.empty_like(t) for t in (self.q[0], self.k[0], self.v[0], self.out, self.lse)]
+                     for _ in range(2)]
+        self.h_out = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (self.out, self.lse)]
+                      for _ in range(2)]
+        nq, nk = self.q1[0].numel(), self.k1[0].numel()
+        self.tok_split = (nq, nq + nk, nq + 2 * nk)
+        tok = torch.cat([torch.cat([self.q1[l].reshape(-1), self.k1[l].reshape(-1), self.v1[l].reshape(-1)])
+                         for l in range(self.layers)])
+        self.tok_words = nq + 2 * nk
+        self.h_tok = tok.cpu().pin_memory()
+        self.d_tok = torch.empty_like(tok)
+        no, nl = self.out1.numel(), self.lse1.numel()    # out bf16, lse fp32 (2 bf16 slots each)
+        self.tokout_words = no + 2 * nl
+        self.d_tokout = torch.empty(self.tokout_words * self.layers, dtype=torch.bfloat16, device=tok.device)
+        self.h_tokout = torch.empty(self.d_tokout.numel(), dtype=torch.bfloat16).pin_memory()
         self.streams = [torch.cuda.Stream() for _ in range(3)]        # upload, kernels, download
         self.ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "done", "out")}
-        self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.h_in)
-        self.d2h_bytes = sum(t.numel() * t.element_size() for t in self.h_out[0])
+        self.ev_tok = {k: torch.cuda.Event() for k in ("in", "done", "out")}
+        self.h2d_bytes = (self.layers * sum(t.numel() * t.element_size() for t in self.h_in)
+                          + self.h_tok.numel() * 2)
+        self.d2h_bytes = (self.layers * sum(t.numel() * t.element_size() for t in self.h_out[0])
+                          + self.h_tokout.numel() * 2)
 
     def run_e2e_steps(self, n):
         """n steps through the C ABI with host buffers; returns CUDA events
@@ -239,60 +296,77 @@ class PrefillStep:
         for st_ in self.streams:
             st_.wait_event(start)
         c = self.cache
-        for i in range(n):
-            b = i % 2
-            q, k, v, q1, k1, v1, out, lse, out1, lse1 = self.dev[b]
+        a, b_, e_ = self.tok_split
+        no, wi, wo = self.out1.numel(), self.tok_words, self.tokout_words
+        g = 0
+        for step in range(n):
             with torch.cuda.stream(sh):
-                if i >= 2:
-                    sh.wait_event(self.ev["done"][b])      # step i-2 has read these inputs
-                for d, h in zip((q, k, v, q1, k1, v1), self.h_in):
-                    d.copy_(h, non_blocking=True)
-                self.ev["in"][b].record(sh)
-            sc.wait_event(self.ev["in"][b])
-            if i >= 2:
-                sc.wait_event(self.ev["out"][b])           # step i-2's outputs are home
-            c.prefill(0, [b], [0, self.L], q, k, v, out, lse, stream=sc)
-            c.append_kv(0, [b], [0, self.L], k, v, stream=sc)
-            c.append_kv(0, [b], [0, 1], k1, v1, stream=sc)
-            c.decode(0, [b], q1, out1, lse1, stream=sc)
-            c.release(b, stream=sc)
-            self.ev["done"][b].record(sc)
-            sd.wait_event(self.ev["done"][b])
+                if step >= 1:
+                    sh.wait_event(self.ev_tok["done"])          # last step's tokens are read
+                self.d_tok.copy_(self.h_tok, non_blocking=True)
+                self.ev_tok["in"].record(sh)
+            for l in range(self.layers):
+                b = g % 2
+                q, k, v, out, lse = self.dset[b]
+                with torch.cuda.stream(sh):
+                    if g >= 2:
+                        sh.wait_event(self.ev["done"][b])      # layer g-2 has read these inputs
+                    for d, h in zip((q, k, v), self.h_in):
+                        d.copy_(h, non_blocking=True)
+                    self.ev["in"][b].record(sh)
+                sc.wait_event(self.ev["in"][b])
+                if g >= 2:
+                    sc.wait_event(self.ev["out"][b])           # layer g-2's outputs are home
+                c.prefill(l, [0], [0, self.L], q, k, v, out, lse, stream=sc)
+                c.append_kv(l, [0], [0, self.L], k, v, stream=sc)
+                self.ev["done"][b].record(sc)
+                sd.wait_event(self.ev["done"][b])
+                with torch.cuda.stream(sd):
+                    for h, d in zip(self.h_out[b], (out, lse)):
+                        h.copy_(d, non_blocking=True)
+                    self.ev["out"][b].record(sd)
+                g += 1
+            sc.wait_event(self.ev_tok["in"])
+            if step >= 1:
+                sc.wait_event(self.ev_tok["out"])               # last step's token outputs are home
+            for l in range(self.layers):
+                ti, to = self.d_tok[l * wi:(l + 1) * wi], self.d_tokout[l * wo:(l + 1) * wo]
+                c.append_kv(l, [0], [0, 1], ti[a:b_].view(self.k1[0].shape),
+                            ti[b_:e_].view(self.v1[0].shape), stream=sc)
+                c.decode(l, [0], ti[:a].view(self.q1[0].shape), to[:no].view(self.out1.shape),
+                         to[no:].view(torch.float32).view(self.lse1.shape), stream=sc)
+            c.release(0, stream=sc)
+            self.ev_tok["done"].record(sc)
+            sd.wait_event(self.ev_tok["done"])
             with torch.cuda.stream(sd):
-                for h, d in zip(self.h_out[b], (out, lse, out1, lse1)):
-                    h.copy_(d, non_blocking=True)
-                self.ev["out"][b].record(sd)
+                self.h_tokout.copy_(self.d_tokout, non_blocking=True)
+                self.ev_tok["out"].record(sd)
         for st_ in self.streams:
             cur.wait_stream(st_)
         end.record(cur)
         return start, end
 
-    # CPU oracle sample of the same workload: rows spread over the sequence
-    def oracle_sample(self, layer_policies, target_s: float, threads: int):
+    def free_e2e(self):
+        for name in ("h_in", "dset", "h_out", "h_tok", "d_tok", "d_tokout", "h_tokout"):
+            if hasattr(self, name):
+                delattr(self, name)
+
+    def oracle_rows(self, layer, rows, threads):
+        """The fp32 C oracle on the given query rows (all heads) of one layer;
+        returns (seconds, visible-pair FLOP)."""
         import oracle
         from oracle import accounting
         pt = [(p.kind, p.sink, p.window, None if p.idx is None else p.idx.tolist())
-              for p in layer_policies]
-        qf = self.q.float().cpu().numpy()
-        kf = self.k.float().cpu().numpy()
-        vf = self.v.float().cpu().numpy()
-        L = self.L
-        rng = np.random.default_rng(5)
-
-        def run_rows(nrows):
-            rows = np.sort(rng.choice(L, size=nrows, replace=False))
-            t0 = time.perf_counter()
-            oracle.attend(qf[rows], kf, vf, rows, pt, "f32", threads=threads)
-            dt = time.perf_counter() - t0
-            pairs = 0
-            grp = self.wl.hq // self.wl.hkv
-            for p in pt:
-                pairs += grp * int(accounting.vis_count_closed(p[0], p[1], p[2], p[3], rows).sum())
-            return dt, 4 * self.wl.d * pairs, nrows
-
-        dt, fl, n = run_rows(16)
-        n2 = int(min(L, max(16, 16 * target_s / max(dt, 1e-3))))
-        return run_rows(n2), qf, kf, vf, pt
+              for p in self.pols[layer]]
+        qf = self.q[layer][rows].float().cpu().numpy()
+        kf = self.k[layer].float().cpu().numpy()
+        vf = self.v[layer].float().cpu().numpy()
+        t0 = time.perf_counter()
+        oracle.attend(qf, kf, vf, rows, pt, "f32", threads=threads)
+        dt = time.perf_counter() - t0
+        grp = self.wl.hq // self.wl.hkv
+        pairs = sum(grp * int(accounting.vis_count_closed(p[0], p[1], p[2], p[3], rows).sum()) for p in pt)
+        return dt, 4 * self.wl.d * pairs
 
 
 FP8_SCALE = 5.6 / 448.0
@@ -422,14 +496,16 @@ class DecodeStep:
         return start, end, work
 
     def run(self, ev_pf=None):
+        """One step; ev_pf (optional): a (start, end) event pair per layer
+        recorded around that layer's decode launch."""
         c = self.cache
         for l in range(self.layers):
             c.append_kv(l, self.seqs, self.cu, self.kn, self.vn)
-            if ev_pf is not None and l == 0:
-                ev_pf[0].record()
+            if ev_pf is not None:
+                ev_pf[l][0].record()
             c.decode(l, self.seqs, self.qs, self.out, self.lse)
-            if ev_pf is not None and l == 0:
-                ev_pf[1].record()
+            if ev_pf is not None:
+                ev_pf[l][1].record()
         self.t += 1
 
 
@@ -451,9 +527,8 @@ def load_traffic(kernel: str, workload: str):
 
 
 def bench_layer(wl) -> int:
-    """The prefill step runs one layer: the first whose policy has a GLOBAL KV
-    head (every layer has the same shapes; this one carries the full-causal
-    work), else layer 0."""
+    """The layer --op chunk_prefill runs: the first whose policy has a GLOBAL
+    KV head (it carries the full-causal work), else layer 0."""
     pols = W.policies(wl)
     return next((l for l, row in enumerate(pols) if any(p.kind == W.GLOBAL for p in row)), 0)
 
@@ -468,7 +543,159 @@ def source_sha():
     return h.hexdigest()[:12]
 
 
+METRIC = "SegPaged prefill TFLOP/s & decode visible-KV GB/s, % of GB300 roofline"
+DATA = "synthetic (seeded N(0,1), pages' shapes)"
+DECODE_WL = "llama3_8b_decode_32k"
+
+
+def is_decode(wl) -> bool:
+    return wl.decode_steps > 0 and wl.name.startswith("llama3_8b")
+
+
+def gpu_uuid():
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(0).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
 # ---------------------------------------------------------------- main arms
+
+def timed_steps(st, steps, warmup, ws, rank, decode):
+    """warmup untimed steps, then `steps` timed ones bracketed by a barrier
+    and a synchronize; L2 is flushed before each step outside its events.
+    Returns the step times, the dominant kernel's summed launch times per
+    step, the work per step (and of those launches) and the clock record."""
+    import torch
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    for _ in range(warmup):
+        st.run()
+    torch.cuda.synchronize()
+    assert st.cache.status() == 0
+    E = lambda: torch.cuda.Event(enable_timing=True)
+    ev = [(E(), E()) for _ in range(steps)]
+    evk = [[(E(), E()) for _ in range(st.layers)] for _ in range(steps)]
+    work, kern_work = [], []
+    clocks = ClockSampler(gpu_uuid() if rank == 0 else None)
+    if rank == 0:
+        clocks.start()
+        time.sleep(0.4)
+    barrier(ws)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush.random_(0, 255) if i == 0 else flush.fill_(i & 0xFF)
+        if decode:
+            work.append(st.step_bytes(st.t))
+            kern_work.append(work[-1])                   # every layer's decode launch
+        else:
+            work.append(st.work)
+            kern_work.append(st.prefill_flop)             # every layer's prefill launch
+        ev[i][0].record(stream)
+        st.run(evk[i])
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clk = clocks.stop() if rank == 0 else None
+    assert st.cache.status() == 0
+    del flush
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    kern_ms = [sum(a.elapsed_time(b) for a, b in row) for row in evk]
+    return step_ms, kern_ms, work, kern_work, clk
+
+
+def prefill_record(args, wl, ws, rank, steps):
+    import torch
+    st = PrefillStep(wl)
+    torch.cuda.synchronize()
+    step_ms, kern_ms, work, kern_work, clk = timed_steps(st, steps, args.warmup, ws, rank, False)
+    total_ms = reduce_max(float(sum(step_ms)), ws)
+    value = job_rate(float(sum(work)), float(sum(step_ms)), ws) * 1e-12
+    # end to end through the same C-ABI calls with host buffers
+    st.setup_e2e()
+    st.run_e2e_steps(1)
+    torch.cuda.synchronize()
+    e2e_steps = 3 if st.layers > 1 else max(3, min(steps, 10))
+    barrier(ws)
+    e0, e1 = st.run_e2e_steps(e2e_steps)
+    torch.cuda.synchronize()
+    assert st.cache.status() == 0
+    e2e = {"value": job_rate(float(st.work * e2e_steps), e0.elapsed_time(e1), ws) * 1e-12,
+           "unit": "TFLOP/s", "h2d_bytes_per_step": st.h2d_bytes, "d2h_bytes_per_step": st.d2h_bytes,
+           "steps": e2e_steps}
+    st.free_e2e()
+    rec = None
+    if rank == 0:
+        peaks, src = load_peaks()
+        launch_ms = float(np.sum(kern_ms)) / (steps * st.layers)
+        achieved = float(np.sum(kern_work)) / (float(np.sum(kern_ms)) / 1e3) / 1e12
+        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": load_traffic("k_prefill", wl.name),
+                "kernel": "k_prefill", "peak_source": src + " bf16_tflops (burst)",
+                "launches_per_step": st.layers,
+                "algorithmic_flop_per_launch": st.prefill_flop / st.layers,
+                "avg_launch_ms": launch_ms}
+        cpu = None
+        if ws == 1 and not args.no_cpu_baseline:
+            cpu = prefill_cpu_baseline(st)
+        rec = {"value": value, "unit": "TFLOP/s", "steps": steps, "ms_per_step": total_ms / steps,
+               "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+               "gpu_launches": st.kernels_per_step * steps, "clocks": clk}
+    st.cache.close()
+    del st
+    import gc
+    gc.collect()
+    torch.cuda.empty_cache()
+    return rec
+
+
+def decode_record(args, wl, ws, rank, steps):
+    import torch
+    fp8 = args.kv_dtype == "fp8"
+    st = DecodeStep(wl, layers=args.decode_layers or None, fp8=fp8)
+    step_ms, kern_ms, work, kern_work, clk = timed_steps(st, steps, args.warmup, ws, rank, True)
+    total_ms = reduce_max(float(sum(step_ms)), ws)
+    value = job_rate(float(sum(work)), float(sum(step_ms)), ws) * 1e-9
+    st.setup_e2e()
+    st.run_e2e_steps(1)
+    torch.cuda.synchronize()
+    barrier(ws)
+    e0, e1, w = st.run_e2e_steps(3)
+    torch.cuda.synchronize()
+    assert st.cache.status() == 0
+    e2e = {"value": job_rate(float(w), e0.elapsed_time(e1), ws) * 1e-9, "unit": "GB/s",
+           "h2d_bytes_per_step": st.h2d_bytes, "d2h_bytes_per_step": st.d2h_bytes, "steps": 3}
+    rec = None
+    if rank == 0:
+        peaks, src = load_peaks()
+        achieved = float(np.sum(kern_work)) / (float(np.sum(kern_ms)) / 1e3) / 1e9
+        peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak,
+                "traffic": load_traffic("k_decode", wl.name + ("_fp8" if fp8 else "")),
+                "kernel": "k_decode", "peak_source": src + " hbm_gbs",
+                "launches_per_step": st.layers,
+                "algorithmic_bytes_per_launch": float(np.mean(kern_work)) / st.layers,
+                "avg_launch_ms": float(np.sum(kern_ms)) / (steps * st.layers)}
+        cpu = None
+        if ws == 1 and not args.no_cpu_baseline:
+            cpu = decode_cpu_baseline(st, wl)
+        rec = {"value": value, "unit": "GB/s", "steps": steps, "warmup": args.warmup,
+               "ms_per_step": total_ms / steps,
+               "dtype": "e4m3 K/V pages, f16 MMA" if fp8 else "bf16",
+               "config": config_dict(wl, args),
+               "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+               "gpu_launches": st.kernels_per_step * steps, "clocks": clk}
+    st.cache.close()
+    del st
+    import gc
+    gc.collect()
+    torch.cuda.empty_cache()
+    return rec
+
 
 def run_ours(args, ws, rank):
     import torch
@@ -478,223 +705,114 @@ def run_ours(args, ws, rank):
     barrier(ws)
     torch.cuda.init()
     wl = W.WORKLOADS[args.workload]
-    decode = wl.decode_steps > 0 and wl.name.startswith("llama3_8b")
+    decode = is_decode(wl)
     if args.kv_dtype == "fp8" and not decode:
         raise SystemExit("--kv-dtype fp8 applies to the decode workload and --op chunk_prefill "
                          "(the prefill step has no cached history)")
+    steps = args.steps
     if decode:
-        st = DecodeStep(wl, layers=args.decode_layers or None, fp8=args.kv_dtype == "fp8")
+        rec = decode_record(args, wl, ws, rank, steps)
     else:
-        layer = bench_layer(wl)
-        st = PrefillStep(wl, W.policies(wl)[layer])
-    stream = torch.cuda.current_stream()
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
-    for _ in range(args.warmup):
-        st.run()
-    torch.cuda.synchronize()
-    assert st.cache.status() == 0
-
-    n_steps = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(n_steps)]
-    evk = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(n_steps)]
-    work = []
-    kern_work = []
-    props = torch.cuda.get_device_properties(0)
-    uuid = None
-    try:
-        u = str(props.uuid)
-        uuid = u if u.startswith("GPU-") else "GPU-" + u
-    except Exception:
-        pass
-    clocks = ClockSampler(uuid if rank == 0 else None)
-    if rank == 0:
-        clocks.start()
-        time.sleep(0.4)
-    barrier(ws)
-    torch.cuda.synchronize()
-    for i in range(n_steps):
-        flush.random_(0, 255) if i == 0 else flush.fill_(i & 0xFF)
-        if decode:
-            work.append(st.step_bytes(st.t))
-            kern_work.append(st.cache.count_decode_bytes(0, st.seqs, [st.t] * st.B))
-        else:
-            work.append(st.work)
-            kern_work.append(st.prefill_flop)
-        ev[i][0].record(stream)
-        st.run(evk[i])
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    barrier(ws)
-    clk = clocks.stop() if rank == 0 else None
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    kern_ms = [a.elapsed_time(b) for a, b in evk]
-    total_ms = reduce_max(float(sum(step_ms)), ws)
-    assert st.cache.status() == 0
-    scale = 1e-12 if not decode else 1e-9
-    value = job_rate(float(sum(work)), float(sum(step_ms)), ws) * scale
-
-    # end-to-end through the same C-ABI calls with host buffers (prefill only)
-    e2e = None
-    if not decode:
-        st.setup_e2e()
-        st.run_e2e_steps(2)
-        torch.cuda.synchronize()
-        e2e_steps = max(3, min(n_steps, 10))
-        barrier(ws)
-        e0, e1 = st.run_e2e_steps(e2e_steps)
-        torch.cuda.synchronize()
-        assert st.cache.status() == 0
-        e2e = {"value": job_rate(float(st.work * e2e_steps), e0.elapsed_time(e1), ws) * scale,
-               "unit": st.unit,
-               "h2d_bytes_per_step": st.h2d_bytes, "d2h_bytes_per_step": st.d2h_bytes}
-    else:
-        st.setup_e2e()
-        st.run_e2e_steps(1)
-        torch.cuda.synchronize()
-        barrier(ws)
-        e0, e1, w = st.run_e2e_steps(3)
-        torch.cuda.synchronize()
-        assert st.cache.status() == 0
-        e2e_rate = job_rate(float(w), e0.elapsed_time(e1), ws)
-        bytes_in, bytes_out = st.h2d_bytes, st.d2h_bytes
-        e2e = {"value": e2e_rate * scale, "unit": st.unit,
-               "h2d_bytes_per_step": bytes_in, "d2h_bytes_per_step": bytes_out}
-
+        rec = prefill_record(args, wl, ws, rank, steps)
+        if wl.layers > 1 and not args.no_decode_record:
+            # the decode half of the metric: the Llama-3-8B-shaped decode
+            # batch at its configuration's 64 steps
+            drec = decode_record(args, W.WORKLOADS[DECODE_WL], ws, rank, 64)
+            if rank == 0:
+                drec["workload"] = DECODE_WL
+                drec["metric"] = "decode visible-KV GB/s"
+                rec["decode"] = drec
     if rank != 0:
         return None
-    peaks, src = load_peaks()
-    kern_avg_ms = float(np.mean(kern_ms))
-    if decode:
-        achieved = float(np.mean(kern_work)) / (kern_avg_ms / 1e3) / 1e9
-        peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak,
-                "traffic": load_traffic("k_decode", wl.name + ("_fp8" if st.fp8 else "")),
-                "kernel": "k_decode", "peak_source": src + " hbm_gbs",
-                "algorithmic_bytes_per_launch": int(np.mean(kern_work)),
-                "avg_launch_ms": kern_avg_ms}
-    else:
-        achieved = st.prefill_flop / (kern_avg_ms / 1e3) / 1e12
-        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": load_traffic("k_prefill", wl.name),
-                "kernel": "k_prefill", "peak_source": src + " bf16_tflops (burst)",
-                "algorithmic_flop_per_launch": st.prefill_flop, "avg_launch_ms": kern_avg_ms}
-
-    cpu = None
-    if ws == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(st, wl, decode)
-    line = {
-        "metric": "SegPaged prefill TFLOP/s & decode visible-KV GB/s, % of GB300 roofline",
-        "value": value, "unit": st.unit, "n_gpus": ws, "steps": n_steps, "warmup": args.warmup,
-        "ms_per_step": total_ms / n_steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "e4m3 K/V pages, f16 MMA" if decode and st.fp8 else "bf16",
-        "data": "synthetic (seeded N(0,1), pages' shapes)",
-        "config": config_dict(wl, decode, st),
-        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": st.kernels_per_step * n_steps, "clocks": clk,
-    }
+    line = {"metric": METRIC, "value": rec.pop("value"), "unit": rec.pop("unit"), "n_gpus": ws,
+            "steps": rec.pop("steps"), "warmup": args.warmup, "ms_per_step": rec.pop("ms_per_step"),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": rec.pop("dtype", "bf16"), "data": DATA, "config": rec.pop("config", None)
+            or config_dict(wl, args)}
+    line.update(rec)
     return line
 
 
-def config_dict(wl, decode, st):
-    d = {"workload": wl.name, "hq": wl.hq, "hkv": wl.hkv, "head_dim": wl.d, "page_size": wl.page,
+def config_dict(wl, args):
+    """The workload as the line names it (the reference arm prints the same)."""
+    d = {"workload": wl.name, "layers": wl.layers, "hq": wl.hq, "hkv": wl.hkv, "head_dim": wl.d,
+         "page_size": wl.page, "local": [wl.local_sink, wl.local_window],
+         "global_units": wl.n_global,
          "l2": "flushed between steps (256 MB write outside the timed events)",
          "parallelism": "replicas (no cross-GPU exchange on this path)"}
-    if decode:
-        d.update({"layers": st.layers, "batch": wl.seqs, "cached_tokens": wl.seq_len,
-                  "global_units": wl.n_global, "local": [wl.local_sink, wl.local_window],
+    if is_decode(wl):
+        fp8 = args.kv_dtype == "fp8"
+        d.update({"layers": args.decode_layers or wl.layers, "batch": wl.seqs,
+                  "cached_tokens": wl.seq_len,
                   "step": "all layers: append 1 token/seq + split-KV decode",
-                  "kv_dtype": "fp8_e4m3" if st.fp8 else "bf16"})
-        if st.fp8:
+                  "kv_dtype": "fp8_e4m3" if fp8 else "bf16"})
+        if fp8:
             d["workload"] = wl.name + "_fp8"
             d["kv_scales"] = "%.6g for every channel of K and V" % FP8_SCALE
     else:
-        layer = bench_layer(wl)
-        d.update({"seq_len": wl.seq_len, "layer": layer, "global_kv_heads_in_layer": sum(
-            1 for p in W.policies(wl)[layer] if p.kind == W.GLOBAL),
-                  "local": [wl.local_sink, wl.local_window],
-                  "step": "prefill + trimmed KV write + 1 decode token + release"})
+        d.update({"seq_len": wl.seq_len, "batch": wl.seqs,
+                  "step": "every layer: prefill of the whole sequence + trimmed KV write; then 1 "
+                          "decode token per layer (append + decode); release"})
     return d
 
 
-def cpu_baseline(st, wl, decode, target_s=12.0):
+def prefill_cpu_baseline(st, target_s=12.0, rows_per_head=256):
+    """The fp32 C oracle on all host cores: 256 sampled query rows (every
+    query head) per layer, layer after layer until about target_s seconds of
+    oracle time; plus a smaller sample on one thread."""
     threads = os.cpu_count() or 1
-    if decode:
-        import oracle
-        # layer 0 of two sequences, one decode query each, K/V regenerated on the host
-        seqs = [0, wl.seqs - 1]
-        busy = 0.0
-        nbytes = 0
-        pt = [(p.kind, p.sink, p.window, None) for p in st.pols[0]]
-        qf = st.qs.float().cpu().numpy()
-        t = st.n - 1
-        k0 = v0 = None
-        for b in seqs:
-            k = W.normal((st.n, wl.hkv, wl.d), W.tensor_seed(0, "k", b, 0)).float().numpy()
-            v = W.normal((st.n, wl.hkv, wl.d), W.tensor_seed(0, "v", b, 0)).float().numpy()
-            if b == 0:
-                k0, v0 = k, v
-            t1 = time.perf_counter()
-            oracle.attend(qf[b:b + 1], k, v, [t], pt, "f32", threads=threads)
-            busy += time.perf_counter() - t1
-            nbytes += st.cache.count_decode_bytes(0, [b], [t])
-        # the same query of sequence 0 on one thread
-        t1 = time.perf_counter()
-        oracle.attend(qf[0:1], k0, v0, [t], pt, "f32", threads=1)
-        one = {"value": st.cache.count_decode_bytes(0, [0], [t]) / (time.perf_counter() - t1) / 1e9,
-               "cores": 1, "sample": "layer 0, sequence 0, one decode query"}
-        return {"value": nbytes / busy / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-                "sample": "layer 0, sequences 0 and %d, one decode query each over %d cached "
-                          "tokens (fp32 C oracle)" % (wl.seqs - 1, st.n), "one_thread": one}
-    (dt, fl, n), *_ = st.oracle_sample(W.policies(wl)[0], target_s, threads)
-    (dt1, fl1, n1), *_ = st.oracle_sample(W.policies(wl)[0], target_s / threads, 1)
-    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": "%d of %d query rows (all %d heads), fp32 C oracle" % (n, st.L, wl.hq),
+    rng = np.random.default_rng(5)
+    n = min(rows_per_head, st.L)
+    busy = flop = 0.0
+    done = []
+    for l in range(st.layers):
+        rows = np.sort(rng.choice(st.L, size=n, replace=False))
+        dt, fl = st.oracle_rows(l, rows, threads)
+        busy += dt
+        flop += fl
+        done.append(l)
+        if busy >= target_s:
+            break
+    rows1 = np.sort(rng.choice(st.L, size=max(4, n // 64), replace=False))
+    dt1, fl1 = st.oracle_rows(0, rows1, 1)
+    return {"value": flop / busy / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": "%d sampled query rows of every query head on %d of %d layers (layers %d-%d), "
+                      "fp32 C oracle" % (n, len(done), st.layers, done[0], done[-1]),
             "one_thread": {"value": fl1 / dt1 / 1e12, "cores": 1,
-                           "sample": "%d of %d query rows (all %d heads)" % (n1, st.L, wl.hq)}}
+                           "sample": "%d query rows of layer 0 (all %d heads)" % (len(rows1), st.wl.hq)}}
 
 
-def run_reference(args, ws, rank):
-    """The CPU oracle as the reference arm: each step one bounded sample."""
-    if ws > 1 and rank != 0:
-        return None
+def decode_cpu_baseline(st, wl):
     import oracle
-    from oracle import accounting
-    wl = W.WORKLOADS[args.workload]
     threads = os.cpu_count() or 1
-    decode = wl.name.startswith("llama3_8b")
-    rng = np.random.default_rng(1)
-    if decode:
-        L = wl.seq_len
-        pol = W.policies(wl)[0]
-        pt = [(p.kind, p.sink, p.window, None) for p in pol]
-        k = W.normal((L, wl.hkv, wl.d), W.tensor_seed(0, "k", 0, 0)).float().numpy()
-        v = W.normal((L, wl.hkv, wl.d), W.tensor_seed(0, "v", 0, 0)).float().numpy()
-        q = W.normal((1, wl.hq, wl.d), 11).float().numpy()
-        nb = sum(int(accounting.vis_count_closed(p[0], p[1], p[2], p[3], np.array([L - 1]))[0])
-                 for p in pt) * 2 * wl.d * 2
+    # layer 0 of two sequences, one decode query each, K/V regenerated on the host
+    seqs = [0, wl.seqs - 1]
+    busy = 0.0
+    nbytes = 0
+    pt = [(p.kind, p.sink, p.window, None) for p in st.pols[0]]
+    qf = st.qs.float().cpu().numpy()
+    t = st.n - 1
+    k0 = v0 = None
+    for b in seqs:
+        k = W.normal((st.n, wl.hkv, wl.d), W.tensor_seed(0, "k", b, 0)).float().numpy()
+        v = W.normal((st.n, wl.hkv, wl.d), W.tensor_seed(0, "v", b, 0)).float().numpy()
+        if b == 0:
+            k0, v0 = k, v
+        t1 = time.perf_counter()
+        oracle.attend(qf[b:b + 1], k, v, [t], pt, "f32", threads=threads)
+        busy += time.perf_counter() - t1
+        nbytes += st.cache.count_decode_bytes(0, [b], [t])
+    # the same query of sequence 0 on one thread
+    t1 = time.perf_counter()
+    oracle.attend(qf[0:1], k0, v0, [t], pt, "f32", threads=1)
+    one = {"value": st.cache.count_decode_bytes(0, [0], [t]) / (time.perf_counter() - t1) / 1e9,
+           "cores": 1, "sample": "layer 0, sequence 0, one decode query"}
+    return {"value": nbytes / busy / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": "layer 0, sequences 0 and %d, one decode query each over %d cached "
+                      "tokens (fp32 C oracle)" % (wl.seqs - 1, st.n), "one_thread": one}
 
-        def one():
-            oracle.attend(q, k, v, [L - 1], pt, "f32", threads=threads)
-            return nb
-        unit, scale, sample = "GB/s", 1e-9, "one decode query of one sequence, layer 0, fp32 C oracle"
-    else:
-        L = wl.seq_len
-        pt = [(p.kind, p.sink, p.window, None) for p in W.policies(wl)[bench_layer(wl)]]
-        q, k, v = (t.float().numpy() for t in W.qkv(wl, L, 0, 0))
-        grp = wl.hq // wl.hkv
-        nrows = 48
 
-        def one():
-            rows = np.sort(rng.choice(L, size=nrows, replace=False))
-            oracle.attend(q[rows], k, v, rows, pt, "f32", threads=threads)
-            return 4 * wl.d * sum(grp * int(accounting.vis_count_closed(p[0], p[1], p[2], p[3], rows).sum())
-                                  for p in pt)
-        unit, scale, sample = "TFLOP/s", 1e-12, "48 random query rows (all heads) per step, fp32 C oracle"
+def reference_steps(args, one, unit, scale):
     for _ in range(args.warmup):
         one()
     t0 = time.perf_counter()
@@ -702,15 +820,93 @@ def run_reference(args, ws, rank):
     for _ in range(args.steps):
         work += one()
     dt = time.perf_counter() - t0
-    value = work * scale / dt
-    return {"impl": "reference", "metric": "SegPaged prefill TFLOP/s & decode visible-KV GB/s, % of GB300 roofline",
-            "value": value, "unit": unit, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded N(0,1), pages' shapes)",
-            "config": {"workload": wl.name, "hq": wl.hq, "hkv": wl.hkv, "head_dim": wl.d},
+    return work * scale / dt, dt
+
+
+def reference_decode(args, wl, threads, steps=None):
+    """The oracle on one decode query (all heads) of one Llama-3-8B-shaped
+    sequence of 32,768 cached tokens, layer 0, per step."""
+    import oracle
+    from oracle import accounting
+    L = wl.seq_len
+    pt = [(p.kind, p.sink, p.window, None) for p in W.policies(wl)[0]]
+    k = W.normal((L, wl.hkv, wl.d), W.tensor_seed(0, "k", 0, 0)).float().numpy()
+    v = W.normal((L, wl.hkv, wl.d), W.tensor_seed(0, "v", 0, 0)).float().numpy()
+    q = W.normal((1, wl.hq, wl.d), 11).float().numpy()
+    nb = sum(int(accounting.vis_count_closed(p[0], p[1], p[2], p[3], np.array([L - 1]))[0])
+             for p in pt) * 2 * wl.d * 2
+
+    def one():
+        oracle.attend(q, k, v, [L - 1], pt, "f32", threads=threads)
+        return nb
+    a = argparse.Namespace(**vars(args))
+    if steps is not None:
+        a.steps = steps
+    value, dt = reference_steps(a, one, "GB/s", 1e-9)
+    return value, dt / a.steps * 1e3, a.steps, "one decode query of one sequence, layer 0, fp32 C oracle"
+
+
+def run_reference(args, ws, rank):
+    """The CPU oracle as the reference arm: each step one bounded sample of
+    the same workload, in the same units."""
+    if ws > 1 and rank != 0:
+        return None
+    import oracle
+    from oracle import accounting
+    wl = W.WORKLOADS[args.workload]
+    threads = os.cpu_count() or 1
+    rng = np.random.default_rng(1)
+    extra = {}
+    if is_decode(wl):
+        value, ms, steps, sample = reference_decode(args, wl, threads)
+        unit = "GB/s"
+    else:
+        L = wl.seq_len
+        pols = W.policies(wl)
+        # up to two layers' K/V on the host (the first with a GLOBAL head and
+        # the next), drawn from the workload's seeds; query rows sampled per step
+        l0 = bench_layer(wl)
+        layers = sorted({l0, (l0 + 1) % wl.layers})
+        kv = {}
+        for l in layers:
+            kv[l] = (W.normal((L, wl.hkv, wl.d), W.tensor_seed(0, "k", 0, l), wl.k_scale).float().numpy(),
+                     W.normal((L, wl.hkv, wl.d), W.tensor_seed(0, "v", 0, l)).float().numpy())
+        grp = wl.hq // wl.hkv
+        nrows = 48
+        state = {"i": 0}
+
+        def one():
+            l = layers[state["i"] % len(layers)]
+            state["i"] += 1
+            pt = [(p.kind, p.sink, p.window, None if p.idx is None else p.idx.tolist()) for p in pols[l]]
+            rows = np.sort(rng.choice(L, size=nrows, replace=False))
+            q = W.normal((nrows, wl.hq, wl.d), W.tensor_seed(0, "q", 0, l, state["i"])).float().numpy()
+            oracle.attend(q, kv[l][0], kv[l][1], rows, pt, "f32", threads=threads)
+            return 4 * wl.d * sum(grp * int(accounting.vis_count_closed(p[0], p[1], p[2], p[3], rows).sum())
+                                  for p in pt)
+        value, dt = reference_steps(args, one, "TFLOP/s", 1e-12)
+        ms, steps, unit = dt / args.steps * 1e3, args.steps, "TFLOP/s"
+        sample = "%d random query rows (all heads) per step of layer %s, fp32 C oracle" % (
+            nrows, " / ".join(str(l) for l in layers))
+        if wl.layers > 1 and not args.no_decode_record:
+            dwl = W.WORKLOADS[DECODE_WL]
+            dv, dms, dsteps, dsample = reference_decode(args, dwl, threads, steps=3)
+            extra["decode"] = {"workload": DECODE_WL, "metric": "decode visible-KV GB/s", "value": dv,
+                               "unit": "GB/s", "steps": dsteps, "ms_per_step": dms,
+                               "config": config_dict(dwl, args),
+                               "cpu_baseline": {"value": dv, "unit": "GB/s", "kind": "oracle",
+                                                "cores": threads, "sample": dsample},
+                               "e2e": {"value": dv, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                                       "d2h_bytes_per_step": 0}}
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": ws,
+            "steps": steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": DATA,
+            "config": config_dict(wl, args),
             "cpu_baseline": {"value": value, "unit": unit, "kind": "oracle", "cores": threads,
                              "sample": sample},
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    line.update(extra)
+    return line
 
 
 def stored_rows(pols_row, n: int, seqs: int, page: int) -> int:
@@ -952,13 +1148,15 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None,
-                    help="timed steps (default 20; the decode workload 64, the step count of "
-                         "its configuration)")
-    ap.add_argument("--warmup", type=int, default=5)
+                    help="timed steps (default: 5 for the 64-layer 128K prefill, 64 for the decode "
+                         "workload -- its configuration's step count -- else 20)")
+    ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="mistral7b_prefill_8k",
-                    choices=["mistral7b_prefill_8k", "llama3_8b_decode_32k", "llama33_70b_prefill_128k"])
+    ap.add_argument("--workload", default="llama33_70b_prefill_128k",
+                    choices=["llama33_70b_prefill_128k", "mistral7b_prefill_8k", "llama3_8b_decode_32k"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode-record", action="store_true",
+                    help="multi-layer prefill workload: leave out the decode record")
     ap.add_argument("--decode-layers", type=int, default=0,
                     help="decode workload: run only the first N layers (profiling a small case)")
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
@@ -967,8 +1165,14 @@ def main():
                     help="time one library operation instead of the attention step")
     args = ap.parse_args()
     if args.steps is None:
-        args.steps = 64 if (args.workload == "llama3_8b_decode_32k" and not args.op
-                            and args.impl == "ours") else 20
+        if args.op or args.impl == "reference":
+            args.steps = 20 if args.workload != "llama33_70b_prefill_128k" or args.op else 5
+        elif args.workload == "llama3_8b_decode_32k":
+            args.steps = 64
+        elif args.workload == "llama33_70b_prefill_128k":
+            args.steps = 5
+        else:
+            args.steps = 20
     if args.warmup < 3:
         args.warmup = 3
     if args.op:

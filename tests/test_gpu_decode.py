@@ -98,42 +98,63 @@ def test_decode_repeat_is_stable():
     assert cache.status() == 0
 
 
-def test_decode_llama3_8b_shape_sampled():
-    """Llama-3-8B-shaped decode batch (32 x 32768 cached, 12.5 % GLOBAL units,
-    LOCAL(4, 2048)) at full size on two layers; the oracle checks two
-    sequences per layer."""
+def test_decode_llama3_8b_shape_64_steps_all_layers():
+    """Llama-3-8B-shaped decode batch as the benchmark runs it: 32 layers x
+    32 sequences of 32,768 cached tokens (12.5 % GLOBAL units, LOCAL(4,
+    2048)), 64 decode steps of one token per sequence in every layer, so
+    GLOBAL units cross a page boundary (position 32,768) and LOCAL rings
+    turn over a page.  The oracle checks sequences 0 and 31 in every layer
+    at steps 0 and 63."""
     gpu_ready()
     wl = W.WORKLOADS["llama3_8b_decode_32k"]
-    layers, B, n = 2, wl.seqs, wl.seq_len
-    pols = W.policies(wl)[:layers]
-    pages = B * sum(pm_pages(p, n + 4, wl.page) for row in pols for p in row) + 64
-    cache = _mk(layers, wl.hq, wl.hkv, wl.d, wl.page, B, n + 64, pages, max_batch=B)
-    keep = {}
+    layers, B, n, steps = wl.layers, wl.seqs, wl.seq_len, wl.decode_steps
+    pols = W.policies(wl)
+    pages = B * sum(pm_pages(p, n + steps, wl.page) for row in pols for p in row) + 64
+    cache = _mk(layers, wl.hq, wl.hkv, wl.d, wl.page, B, n + steps + 8, pages, max_batch=B)
+    watched = (0, B - 1)
+    full = {}                       # (b, l) -> whole K / V token streams of watched sequences
+    new_k = [[None] * B for _ in range(layers)]
+    new_v = [[None] * B for _ in range(layers)]
     for b in range(B):
         cache.set_policy(b, to_c_policies(pols))
-        for l in range(layers):
-            k = W.normal((n + 1, wl.hkv, wl.d), 5000 + 100 * b + l, device="cuda")
-            v = W.normal((n + 1, wl.hkv, wl.d), 7000 + 100 * b + l, device="cuda")
-            cache.build(b, l, k[:n], v[:n])
-            if b in (0, B - 1):
-                keep[(b, l)] = (k, v)
-            else:
-                # append the decode token now; sampled sequences below
-                cache.append_kv(l, [b], [0, 1], k[n:].contiguous(), v[n:].contiguous())
-            del k, v
     for l in range(layers):
-        for b in (0, B - 1):
-            k, v = keep[(b, l)]
-            cache.append_kv(l, [b], [0, 1], k[n:].contiguous(), v[n:].contiguous())
-        q = W.normal((B, wl.hq, wl.d), 31 + l, device="cuda")
-        out, lse = cache.decode(l, list(range(B)), q)
-        for b in (0, B - 1):
-            k, v = keep[(b, l)]
-            pt = [pol_tuple(p) for p in pols[l]]
-            ref, lref = oracle.attend(f64(q[b:b + 1]), f64(k), f64(v), [n], pt, "f64",
-                                      threads=ncores())
-            compare(out[b:b + 1], ref, lse[b:b + 1], lref, "layer %d seq %d" % (l, b))
+        for b in range(B):
+            k = W.normal((n + steps, wl.hkv, wl.d), W.tensor_seed(3, "k", b, l), device="cuda")
+            v = W.normal((n + steps, wl.hkv, wl.d), W.tensor_seed(3, "v", b, l), device="cuda")
+            cache.build(b, l, k[:n], v[:n])
+            new_k[l][b], new_v[l][b] = k[n:].clone(), v[n:].clone()
+            if b in watched:
+                full[(b, l)] = (k, v)
+            del k, v
+    torch.cuda.synchronize()
     assert cache.status() == 0
+    seqs = list(range(B))
+    cu = list(range(B + 1))
+    kept = {}
+    for step in range(steps):
+        for l in range(layers):
+            kd = torch.stack([new_k[l][b][step] for b in seqs]).contiguous()
+            vd = torch.stack([new_v[l][b][step] for b in seqs]).contiguous()
+            cache.append_kv(l, seqs, cu, kd, vd)
+            q = W.normal((B, wl.hq, wl.d), W.tensor_seed(3, "q", l, step), device="cuda")
+            out, lse = cache.decode(l, seqs, q)
+            if step in (0, steps - 1):
+                kept[(l, step)] = (q[list(watched)].clone(), out[list(watched)].clone(),
+                                   lse[list(watched)].clone())
+    torch.cuda.synchronize()
+    assert cache.status() == 0
+    for l in range(layers):
+        pt = [pol_tuple(p) for p in pols[l]]
+        for j, b in enumerate(watched):
+            k, v = full[(b, l)]
+            k64, v64 = f64(k), f64(v)
+            for step in (0, steps - 1):
+                q, out, lse = kept[(l, step)]
+                t = n + step
+                ref, lref = oracle.attend(f64(q[j:j + 1]), k64[:t + 1], v64[:t + 1], [t], pt, "f64",
+                                          threads=ncores())
+                compare(out[j:j + 1], ref, lse[j:j + 1], lref,
+                        "layer %d seq %d step %d" % (l, b, step))
 
 
 def pm_pages(p, n, P):

@@ -200,27 +200,48 @@ def test_prefill_rejects_out_not_32_byte_aligned():
     assert cache.status() == 0
 
 
-def test_llama33_70b_shape_sampled():
-    """Llama-3.3-70B-shaped layer at full size: Hq 64 / Hkv 8, d 128, L 131072,
-    LOCAL(4, 8192) and GLOBAL heads, one-shot causal prefill of one layer in the
-    launch configuration the benchmark uses; the oracle checks 24 sampled rows
-    per query head (first, last, window edges, random)."""
+def _unit_pages(p, n, P):
+    from oracle import pagemodel
+    return pagemodel.pages_needed(p.kind, p.sink, p.window,
+                                  None if p.idx is None else [int(x) for x in p.idx], n, P)
+
+
+def test_llama33_70b_shape_all_layers_sampled():
+    """Llama-3.3-70B-shaped long prefill as the benchmark runs it: all 64
+    layers, each with its own policy row (77 of the 512 (layer, KV head)
+    units GLOBAL by seed, the rest LOCAL(4, 8192)) and its own Q/K/V,
+    Hq 64 / Hkv 8, d 128, one sequence of 131,072 tokens prefilled as one
+    chunk per layer and then written to the cache.  256 sampled query rows
+    of every query head of every layer (the first and last rows and the
+    window edges among them) are checked against the row-sampled oracle."""
     gpu_ready()
+    from oracle import rows as orows
     wl = W.WORKLOADS["llama33_70b_prefill_128k"]
-    Lq = wl.seq_len
-    pols_all = W.policies(wl)
-    layer = next(l for l, row in enumerate(pols_all) if any(p.kind == G for p in row))
-    pols = [pols_all[layer]]
-    cache = _mk(1, wl.hq, wl.hkv, wl.d, wl.page, 1, Lq, 8 * (Lq // wl.page + 2))
+    Lq, n_rows = wl.seq_len, 256
+    pols = W.policies(wl)
+    pages = sum(_unit_pages(p, Lq, wl.page) for row in pols for p in row) + 64
+    cache = _mk(wl.layers, wl.hq, wl.hkv, wl.d, wl.page, 1, Lq + 64, pages, max_batch=1,
+                max_idx=1, max_tokens=Lq)
     cache.set_policy(0, to_c_policies(pols))
-    q, k, v = W.qkv(wl, Lq, 0, layer, device="cuda")
-    out, lse = cache.prefill(0, [0], [0, Lq], q, k, v)
+    out = torch.empty(Lq, wl.hq, wl.d, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(Lq, wl.hq, dtype=torch.float32, device="cuda")
     rng = np.random.default_rng(11)
-    rows = np.unique(np.concatenate([[0, 1, 127, 128, 8191, 8192, 8195, Lq - 129, Lq - 1],
-                                     rng.integers(0, Lq, 15)]))
-    pt = [pol_tuple(p) for p in pols[0]]
-    ref, lref = oracle.attend(f64(q[rows]), f64(k), f64(v), rows, pt, "f64", threads=ncores())
-    compare(out[rows], ref, lse[rows], lref, "llama-70B-shaped layer %d" % layer)
+    fixed = np.array([0, 1, 127, 128, 8191, 8192, 8195, Lq - 129, Lq - 1])
+    torch.set_num_threads(ncores())
+    for l in range(wl.layers):
+        q, k, v = W.qkv(wl, Lq, 0, l, device="cuda")
+        cache.prefill(l, [0], [0, Lq], q, k, v, out, lse)
+        cache.append_kv(l, [0], [0, Lq], k, v)
+        rest = np.setdiff1d(np.arange(Lq), fixed)
+        rows = np.sort(np.concatenate([fixed, rng.choice(rest, n_rows - len(fixed), replace=False)]))
+        ts = torch.as_tensor(rows, device="cuda")
+        pt = [pol_tuple(p) for p in pols[l]]
+        ref, lref = orows.attend_rows(q[ts].float().cpu().numpy(), k.float().cpu().numpy(),
+                                      v.float().cpu().numpy(), rows, pt)
+        compare(out[ts], ref, lse[ts], lref, "llama-70B-shaped layer %d" % l)
+        del q, k, v
+    assert cache.status() == 0
+    cache.release(0)
     assert cache.status() == 0
 
 

@@ -6,8 +6,9 @@ RETRIEVAL (top-2048 indices from seeded scores).  Schedule (the reading of
 the unstated interleaving): every step prefills one 4096-token chunk of the
 lowest-index sequence still prefilling, then decodes one token for every
 sequence whose prefill is done; after all prefills, 16 more decode steps.
-Two of the 32 layers are run (every layer has the same shapes); sampled rows
-of every chunk and sampled decode steps are checked against the oracle.
+All 32 layers are run, each with its own policy rows; at every step the
+oracle checks sampled prefill rows and decode rows of two layers, taken in
+turn, so every layer is checked at several steps.
 """
 import numpy as np
 import pytest
@@ -24,7 +25,7 @@ def test_ragged_mixed_serving_batch():
     gpu_ready()
     from head_aware_paged_gb300 import Config, SegPagedCache
     wl = W.WORKLOADS["ragged_mixed"]
-    layers = 2
+    layers = wl.layers
     lens = W.seq_lengths(wl)
     B, chunk, extra = wl.seqs, wl.chunk, wl.decode_steps
     n_dec_max = sum(-(-L // chunk) for L in lens) + extra + 4
@@ -55,25 +56,24 @@ def test_ragged_mixed_serving_batch():
     rng = np.random.default_rng(3)
     checked = 0
 
-    host = {}
-
-    def kv64(b, l):
-        if (b, l) not in host:
-            host[(b, l)] = (f64(K[(b, l)]), f64(V[(b, l)]))
-        return host[(b, l)]
+    from oracle import rows as orows
 
     def check_rows(b, l, rows, got, lse):
         nonlocal checked
         e = int(rows.max()) + 1
         pt = [pol_tuple(p) for p in pols[b][l]]
-        k64, v64 = kv64(b, l)
-        ref, lref = oracle.attend(f64(Q[(b, l)][torch.as_tensor(rows, device="cuda")]),
-                                  k64[:e], v64[:e], rows, pt, "f64", threads=ncores())
+        k32 = K[(b, l)][:e].float().cpu().numpy()
+        v32 = V[(b, l)][:e].float().cpu().numpy()
+        q32 = Q[(b, l)][torch.as_tensor(rows, device="cuda")].float().cpu().numpy()
+        ref, lref = orows.attend_rows(q32, k32, v32, rows, pt)
         compare(got, ref, lse, lref, "seq %d layer %d rows %s" % (b, l, rows[:3]))
         checked += 1
 
+    torch.set_num_threads(ncores())
+    seen = set()
     step = 0
     while any(held[b] < lens[b] for b in range(B)) or extra > 0:
+        watch = {(2 * step) % layers, (2 * step + 1) % layers}   # layers checked this step
         pre = [b for b in range(B) if held[b] < lens[b]]
         dec = [b for b in range(B) if held[b] >= lens[b]]
         if pre:
@@ -85,10 +85,11 @@ def test_ragged_mixed_serving_batch():
                 kc = K[(b, l)][n0:n0 + c].contiguous()
                 vc = V[(b, l)][n0:n0 + c].contiguous()
                 out, lse = cache.prefill(l, [b], [0, c], qc, kc, vc)
-                if step % 3 == 0 or n0 == 0 or n0 + c == lens[b]:
+                if l in watch:
                     sel = np.unique(np.concatenate([[0, c - 1], rng.integers(0, c, 4)]))
                     ts = torch.as_tensor(sel, device="cuda")
                     check_rows(b, l, n0 + sel, out[ts], lse[ts])
+                    seen.add(l)
                 cache.append_kv(l, [b], [0, c], kc, vc)
             held[b] += c
         if dec:
@@ -98,7 +99,7 @@ def test_ragged_mixed_serving_batch():
                 qd = torch.stack([Q[(b, l)][held[b]] for b in dec]).contiguous()
                 cache.append_kv(l, dec, list(range(len(dec) + 1)), kd, vd)
                 out, lse = cache.decode(l, dec, qd)
-                if step % 5 == 0 or not pre:
+                if l in watch:
                     for n, b in enumerate(dec[:3]):
                         check_rows(b, l, np.array([held[b]]), out[n:n + 1], lse[n:n + 1])
             for b in dec:
@@ -108,3 +109,4 @@ def test_ragged_mixed_serving_batch():
         step += 1
     assert cache.status() == 0
     assert checked > 40
+    assert seen == set(range(layers))
