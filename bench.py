@@ -185,14 +185,16 @@ class PrefillStep:
     pages.  Each layer has its own head-class row and its own Q/K/V, all
     resident in HBM before timing; the policy is set once, offline."""
 
-    def __init__(self, wl, device="cuda"):
+    def __init__(self, wl, device="cuda", layer_range=None):
         import torch
         from head_aware_paged_gb300 import Config, Policy, SegPagedCache
         self.wl = wl
         L = wl.seq_len
         self.L = L
-        self.layers = wl.layers
-        self.pols = W.policies(wl)
+        lo, hi = layer_range or (0, wl.layers)
+        self.layer_ids = list(range(lo, hi))         # the workload's layers this step runs
+        self.layers = hi - lo
+        self.pols = W.policies(wl)[lo:hi]
         pages = sum(unit_pages(p, L + 1, wl.page) for row in self.pols for p in row)
         n_idx = sum(0 if p.idx is None else len(p.idx) for row in self.pols for p in row)
         self.cfg = Config(num_layers=self.layers, num_q_heads=wl.hq, num_kv_heads=wl.hkv,
@@ -205,7 +207,7 @@ class PrefillStep:
                                    for p in row] for row in self.pols])
         # per layer: rows 0..L-1 are the prefill chunk, row L the decode token
         self.q, self.k, self.v, self.q1, self.k1, self.v1 = [], [], [], [], [], []
-        for l in range(self.layers):
+        for l in self.layer_ids:
             q, k, v = W.qkv(wl, L + 1, 0, l, device=device)
             for lst, t in ((self.q, q), (self.k, k), (self.v, v)):
                 lst.append(t[:L])
@@ -608,24 +610,26 @@ def timed_steps(st, steps, warmup, ws, rank, decode):
 
 def prefill_record(args, wl, ws, rank, steps):
     import torch
-    st = PrefillStep(wl)
+    st = PrefillStep(wl, layer_range=layer_range(args, wl))
     torch.cuda.synchronize()
     step_ms, kern_ms, work, kern_work, clk = timed_steps(st, steps, args.warmup, ws, rank, False)
     total_ms = reduce_max(float(sum(step_ms)), ws)
     value = job_rate(float(sum(work)), float(sum(step_ms)), ws) * 1e-12
     # end to end through the same C-ABI calls with host buffers
-    st.setup_e2e()
-    st.run_e2e_steps(1)
-    torch.cuda.synchronize()
-    e2e_steps = 3 if st.layers > 1 else max(3, min(steps, 10))
-    barrier(ws)
-    e0, e1 = st.run_e2e_steps(e2e_steps)
-    torch.cuda.synchronize()
-    assert st.cache.status() == 0
-    e2e = {"value": job_rate(float(st.work * e2e_steps), e0.elapsed_time(e1), ws) * 1e-12,
-           "unit": "TFLOP/s", "h2d_bytes_per_step": st.h2d_bytes, "d2h_bytes_per_step": st.d2h_bytes,
-           "steps": e2e_steps}
-    st.free_e2e()
+    e2e = None
+    if not args.no_e2e:
+        st.setup_e2e()
+        st.run_e2e_steps(1)
+        torch.cuda.synchronize()
+        e2e_steps = 3 if st.layers > 1 else max(3, min(steps, 10))
+        barrier(ws)
+        e0, e1 = st.run_e2e_steps(e2e_steps)
+        torch.cuda.synchronize()
+        assert st.cache.status() == 0
+        e2e = {"value": job_rate(float(st.work * e2e_steps), e0.elapsed_time(e1), ws) * 1e-12,
+               "unit": "TFLOP/s", "h2d_bytes_per_step": st.h2d_bytes,
+               "d2h_bytes_per_step": st.d2h_bytes, "steps": e2e_steps}
+        st.free_e2e()
     rec = None
     if rank == 0:
         peaks, src = load_peaks()
@@ -659,15 +663,17 @@ def decode_record(args, wl, ws, rank, steps):
     step_ms, kern_ms, work, kern_work, clk = timed_steps(st, steps, args.warmup, ws, rank, True)
     total_ms = reduce_max(float(sum(step_ms)), ws)
     value = job_rate(float(sum(work)), float(sum(step_ms)), ws) * 1e-9
-    st.setup_e2e()
-    st.run_e2e_steps(1)
-    torch.cuda.synchronize()
-    barrier(ws)
-    e0, e1, w = st.run_e2e_steps(3)
-    torch.cuda.synchronize()
-    assert st.cache.status() == 0
-    e2e = {"value": job_rate(float(w), e0.elapsed_time(e1), ws) * 1e-9, "unit": "GB/s",
-           "h2d_bytes_per_step": st.h2d_bytes, "d2h_bytes_per_step": st.d2h_bytes, "steps": 3}
+    e2e = None
+    if not args.no_e2e:
+        st.setup_e2e()
+        st.run_e2e_steps(1)
+        torch.cuda.synchronize()
+        barrier(ws)
+        e0, e1, w = st.run_e2e_steps(3)
+        torch.cuda.synchronize()
+        assert st.cache.status() == 0
+        e2e = {"value": job_rate(float(w), e0.elapsed_time(e1), ws) * 1e-9, "unit": "GB/s",
+               "h2d_bytes_per_step": st.h2d_bytes, "d2h_bytes_per_step": st.d2h_bytes, "steps": 3}
     rec = None
     if rank == 0:
         peaks, src = load_peaks()
@@ -733,6 +739,20 @@ def run_ours(args, ws, rank):
     return line
 
 
+def layer_range(args, wl):
+    """--layers: all of the workload's layers (default), the first N ("N") or
+    layers a .. b-1 ("a:b")."""
+    if not args.layers:
+        return (0, wl.layers)
+    if ":" in args.layers:
+        a, b = (int(x) for x in args.layers.split(":"))
+    else:
+        a, b = 0, int(args.layers)
+    if not 0 <= a < b <= wl.layers:
+        raise SystemExit("--layers must select layers inside 0 .. %d" % (wl.layers - 1))
+    return (a, b)
+
+
 def config_dict(wl, args):
     """The workload as the line names it (the reference arm prints the same)."""
     d = {"workload": wl.name, "layers": wl.layers, "hq": wl.hq, "hkv": wl.hkv, "head_dim": wl.d,
@@ -750,6 +770,10 @@ def config_dict(wl, args):
             d["workload"] = wl.name + "_fp8"
             d["kv_scales"] = "%.6g for every channel of K and V" % FP8_SCALE
     else:
+        lo, hi = layer_range(args, wl)
+        if (lo, hi) != (0, wl.layers):
+            d["layers"] = hi - lo
+            d["layer_range"] = [lo, hi]
         d.update({"seq_len": wl.seq_len, "batch": wl.seqs,
                   "step": "every layer: prefill of the whole sequence + trimmed KV write; then 1 "
                           "decode token per layer (append + decode); release"})
@@ -1155,8 +1179,13 @@ def main():
     ap.add_argument("--workload", default="llama33_70b_prefill_128k",
                     choices=["llama33_70b_prefill_128k", "mistral7b_prefill_8k", "llama3_8b_decode_32k"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="leave out the end-to-end leg (short runs and profiling cases)")
     ap.add_argument("--no-decode-record", action="store_true",
                     help="multi-layer prefill workload: leave out the decode record")
+    ap.add_argument("--layers", default="",
+                    help="prefill workload: run the first N layers (\"N\") or layers a..b-1 (\"a:b\") "
+                         "instead of all (short runs and small profiling cases)")
     ap.add_argument("--decode-layers", type=int, default=0,
                     help="decode workload: run only the first N layers (profiling a small case)")
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],

@@ -24,8 +24,10 @@
 //                grew by more than 2^8 (lazy rescale).
 //   The two query tiles share every K/V tile and ping-pong on the tensor core:
 //   while one softmax group works, the MMA warp runs the other's PV and next QK.
-// Work items are assigned to CTAs on the host, longest first, each to the
-// CTA with the least work so far (greedy LPT), so no SM idles at the tail.
+// Work items are assigned to CTAs on the host, one (sequence, KV head) unit
+// after another and longest first within a unit, each to the CTA with the
+// least work so far (greedy), so no SM idles at the tail and the CTAs share
+// one unit's K/V in L2 at a time.
 // Every wait is bounded (sp_device.cuh); on a time-out the CTA drains its
 // copies and MMAs, frees TMEM and returns with the status word set.
 #include <algorithm>
@@ -819,7 +821,7 @@ sp_status prefill_impl(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32
     p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c->cfg.head_dim));
     p.out = out;
     p.lse = lse;
-    struct Cand { int64_t cost; int4 item; };
+    struct Cand { int64_t cost; int32_t unit; int4 item; };   // unit: call sequence * Hkv + KV head
     std::vector<Cand> cands;
     const int P = c->cfg.page_size;
     for (int b = 0; b < n_seqs; ++b) {
@@ -845,16 +847,31 @@ sp_status prefill_impl(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32
                 // item, about three tiles' worth.
                 const int64_t cost = kTileCost * pl.ntiles + kItemCost;
                 for (int pr = 0; pr < pairs; ++pr)
-                    cands.push_back({cost, make_int4(b, h, pr | (rb << 8), (int)pl.ntiles)});
+                    cands.push_back({cost, b * c->cfg.num_kv_heads + h,
+                                     make_int4(b, h, pr | (rb << 8), (int)pl.ntiles)});
             }
         }
     }
     if ((int64_t)cands.size() + (c->num_sms + 4) / 4 > c->ws.max_tiles)
         return fail(SP_ERR_UNSUPPORTED, "prefill work list larger than the workspace");
-    std::stable_sort(cands.begin(), cands.end(),
-                     [](const Cand& a, const Cand& b2) { return a.cost > b2.cost; });
-    // Greedy longest-processing-time assignment: each item, longest first,
-    // goes to the CTA with the least work so far.
+    // Order: unit by unit (units with the most work first), each unit's items
+    // longest first.  All CTAs then work through one unit's K/V at a time
+    // (a GLOBAL head of a 128K sequence holds 67 MB of K and V), instead of
+    // every unit whose items have similar lengths at once, which overflows
+    // L2 and reads K/V tiles from HBM several times.
+    const int n_units = n_seqs * c->cfg.num_kv_heads;
+    std::vector<int64_t> unit_cost(n_units, 0);
+    for (const Cand& cd : cands) unit_cost[cd.unit] += cd.cost;
+    std::vector<int32_t> by_cost(n_units), rank(n_units);
+    for (int u = 0; u < n_units; ++u) by_cost[u] = u;
+    std::stable_sort(by_cost.begin(), by_cost.end(),
+                     [&](int32_t a, int32_t b2) { return unit_cost[a] > unit_cost[b2]; });
+    for (int r = 0; r < n_units; ++r) rank[by_cost[r]] = r;
+    std::stable_sort(cands.begin(), cands.end(), [&](const Cand& a, const Cand& b2) {
+        return rank[a.unit] != rank[b2.unit] ? rank[a.unit] < rank[b2.unit] : a.cost > b2.cost;
+    });
+    // Greedy assignment in that order: each item goes to the CTA with the
+    // least work so far (longest-processing-time rule within a unit).
     const int grid = (int)std::min<int64_t>(c->num_sms, (int64_t)cands.size());
     std::vector<int64_t> load(grid, 0);
     std::vector<std::vector<int4>> per(grid);
