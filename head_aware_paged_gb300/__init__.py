@@ -187,6 +187,30 @@ def sp_select_heavy_hitters(q_obs: torch.Tensor, k: torch.Tensor, topk: int, rec
     return idx, counts, scores
 
 
+def sp_select_heavy_hitters_top_p(q_obs: torch.Tensor, k: torch.Tensor, top_p: float,
+                                  max_keys: int, recent: int = 0, want_scores: bool = False,
+                                  stream=None):
+    """The top-p form of the selection: per KV head the shortest prefix of
+    the ranked candidates whose summed score reaches top_p of their total, at
+    most max_keys, then the recent window.  Returns (idx [Hkv, max_keys +
+    recent] int32 padded with -1, counts [Hkv] int32, scores or None)."""
+    n_obs, hq, d = q_obs.shape
+    n, hkv, _ = k.shape
+    nbytes = c_size_t()
+    check(load().sp_select_workspace_bytes(n_obs, n, hq, hkv, byref(nbytes)))
+    ws = torch.empty(nbytes.value + 256, dtype=torch.uint8, device=k.device)
+    off = (-ws.data_ptr()) % 256
+    idx = torch.empty(hkv, max_keys + recent, dtype=torch.int32, device=k.device)
+    counts = torch.empty(hkv, dtype=torch.int32, device=k.device)
+    scores = torch.empty(hkv, n, dtype=torch.float32, device=k.device) if want_scores else None
+    check(load().sp_select_heavy_hitters_top_p(
+        _ptr(q_obs), n_obs, _ptr(k), n, hq, hkv, d, float(top_p), max_keys, recent,
+        ctypes.cast(idx.data_ptr(), ctypes.POINTER(c_int32)),
+        ctypes.cast(counts.data_ptr(), ctypes.POINTER(c_int32)),
+        _ptr(scores), c_void_p(ws.data_ptr() + off), nbytes.value, _stream(stream)))
+    return idx, counts, scores
+
+
 def sp_set_kv_scales(handle, layer: int, k_scale, v_scale, stream=None) -> None:
     """Per-channel FP8 scales of one layer: host float arrays [Hkv][d]."""
     ks = np.ascontiguousarray(np.asarray(k_scale, dtype=np.float32).reshape(-1))

@@ -23,7 +23,7 @@ EXPORTS = ("sp_required_bytes", "sp_cache_create", "sp_cache_destroy", "sp_set_p
            "sp_build_cache", "sp_append_kv", "sp_attention_prefill", "sp_attention_decode",
            "sp_attention_decode_static_scratch", "sp_rope_realign", "sp_pack_seq",
            "sp_unpack_seq", "sp_select_workspace_bytes", "sp_select_heavy_hitters",
-           "sp_set_kv_scales",
+           "sp_select_heavy_hitters_top_p", "sp_set_kv_scales",
            "sp_release_seq", "sp_export_table", "sp_visible_count", "sp_seq_len",
            "sp_free_pages", "sp_count_prefill_pairs", "sp_count_decode_bytes",
            "sp_get_status", "sp_selftest_bounded_wait", "sp_last_error")
@@ -77,6 +77,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "sp_select_workspace_bytes": [c_int32, c_int32, c_int32, c_int32, POINTER(c_size_t)],
         "sp_select_heavy_hitters": [P, c_int32, P, c_int32, c_int32, c_int32, c_int32, c_int32,
                                     c_int32, I32P, I32P, P, P, c_size_t, P],
+        "sp_select_heavy_hitters_top_p": [P, c_int32, P, c_int32, c_int32, c_int32, c_int32,
+                                          ctypes.c_float, c_int32, c_int32, I32P, I32P, P, P,
+                                          c_size_t, P],
         "sp_set_kv_scales": [P, c_int32, POINTER(ctypes.c_float), POINTER(ctypes.c_float), P],
         "sp_release_seq": [P, c_int32, P],
         "sp_export_table": [P, c_int32, c_int32, c_int32, I32P, I32P, I32P, c_int32, P],

@@ -24,6 +24,9 @@
 //                grew by more than 2^8 (lazy rescale).
 //   The two query tiles share every K/V tile and ping-pong on the tensor core:
 //   while one softmax group works, the MMA warp runs the other's PV and next QK.
+//   The softmax warps of the two tiles take turns K/V tile by K/V tile (an
+//   mbarrier per pair of warps on the same SM sub-partition), so the two
+//   softmaxes never run at once and their MMA blocks never queue together.
 // Work items are assigned to CTAs on the host, one (sequence, KV head) unit
 // after another and longest first within a unit, each to the CTA with the
 // least work so far (greedy), so no SM idles at the tail and the CTAs share
@@ -200,7 +203,8 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
     uint64_t* p_full = s_full + 2;                    // [2]
     uint64_t* o_full = p_full + 2;                    // [2]
     uint64_t* o_empty = o_full + 2;                   // [2]
-    uint64_t* mma_done = o_empty + 2;
+    uint64_t* turn = o_empty + 2;                     // [2 tiles][4 warps] softmax hand-overs
+    uint64_t* mma_done = turn + 8;
     uint64_t* f_full = mma_done + 1;                  // [2] FP8 code slot landed
     uint64_t* f_empty = f_full + 2;                   // [2] FP8 code slot converted
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(f_empty + 2);
@@ -235,6 +239,7 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
             mbar_init(&o_full[t], 1);
             mbar_init(&o_empty[t], 4);
         }
+        for (int x = 0; x < 8; ++x) mbar_init(&turn[x], 1);
         mbar_init(mma_done, 1);
         for (int f = 0; f < 2; ++f) { mbar_init(&f_full[f], 1); mbar_init(&f_empty[f], 1); }
         *abort_flag = 0;
@@ -576,6 +581,16 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                                                                   lane + 32 * q4, P);
                     }
                     if (!mbar_wait(&s_full[t], k & 1, abort_flag, status)) { ok = false; break; }
+                    // The two query tiles take turns: this warp's partner in
+                    // the other tile runs on the same SM sub-partition, and if
+                    // their softmaxes overlap both slow down and then both MMA
+                    // blocks queue on the tensor core at once.  So tile 1
+                    // starts K/V tile k after its partner handed over P of k,
+                    // and tile 0 starts k after its partner handed over k - 1;
+                    // each softmax then runs while the other tile's MMAs do.
+                    if (nq > 1 && (t == 1 || k > 0) &&
+                        !mbar_wait(&turn[(1 - t) * 4 + (warp & 3)], (t == 1 ? k : k - 1) & 1,
+                                   abort_flag, status)) { ok = false; break; }
                     tc_fence_after();
                     // Visibility bits of this row for columns 0..127.  Chunk tiles
                     // (affine positions p = start + c): c < nvalid, c <= i - start,
@@ -697,7 +712,10 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                     tmem_st_wait();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&p_full[t]);
+                    if (lane == 0) {
+                        mbar_arrive(&p_full[t]);
+                        if (nq > 1) mbar_arrive(&turn[t * 4 + (warp & 3)]);
+                    }
                     // the row sum is not needed by the MMA: fold it after the arrive
                     float rsum[8];
                     #pragma unroll

@@ -19,6 +19,12 @@
 //   4. k_hh_topk: per KV head, a radix select of the topk-th largest score
 //      (scores are >= 0, so their bit patterns order like the values), then
 //      the selected indices compacted in index order.
+// The top-p form (sp_select_heavy_hitters_top_p) first runs k_hh_topp_count:
+// per KV head, how many of the highest-ranked candidates (score descending,
+// index ascending) it takes for their summed score to reach top_p times the
+// candidates' total (at most max_keys), found by the same digit-by-digit
+// descent with each bucket's score mass summed in float64; k_hh_topk then
+// selects that many keys per head.
 #include <cmath>
 #include <memory>
 
@@ -211,14 +217,102 @@ __global__ void k_hh_rows(const __grid_constant__ HhParams p) {
     p.row_l[r] = L;
 }
 
-// Top-k per KV head: radix select on the score bits, compaction in index order.
+// Top-p count per KV head: the smallest m such that the m highest-ranked
+// candidates (j < n - recent; score descending, index ascending) hold at
+// least top_p times the candidates' total score, capped at max_keys; 0 when
+// that target is 0.  The threshold score T is found digit by digit from the
+// top (8 bits at a time) with each bucket's key count and float64 score mass;
+// the keys above T are all taken, then as many keys equal to T as the target
+// still needs.
 __global__ void __launch_bounds__(kHhTopkThreads)
-k_hh_topk(const float* scores, int32_t n, int32_t topk, int32_t recent, int32_t* idx,
-          int32_t* counts) {
+k_hh_topp_count(const float* scores, int32_t n, float top_p, int32_t max_keys, int32_t recent,
+                int32_t* kk_out) {
+    const int h = blockIdx.x;
+    const float* sc = scores + (int64_t)h * n;
+    const uint32_t* key = reinterpret_cast<const uint32_t*>(sc);
+    const int ncand = max(n - recent, 0);
+    __shared__ double wsum[kHhTopkThreads / 32];
+    __shared__ uint32_t hcnt[256];
+    __shared__ double hmass[256];
+    __shared__ uint32_t s_prefix, s_cabove;
+    __shared__ double s_above, s_target;
+    // the candidates' total score (fixed reduction order)
+    double t = 0.0;
+    for (int j = threadIdx.x; j < ncand; j += blockDim.x) t += (double)sc[j];
+    #pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = t;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double tot = 0.0;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += wsum[w];
+        s_target = (double)top_p * tot;
+    }
+    __syncthreads();
+    const double target = s_target;
+    if (ncand == 0 || !(target > 0.0)) {
+        if (threadIdx.x == 0) kk_out[h] = 0;
+        return;
+    }
+    uint32_t prefix = 0, mask = 0, cabove = 0;   // keys above the current prefix range
+    double above = 0.0;                          // and their score mass
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int b = threadIdx.x; b < 256; b += blockDim.x) { hcnt[b] = 0; hmass[b] = 0.0; }
+        __syncthreads();
+        for (int j = threadIdx.x; j < ncand; j += blockDim.x) {
+            const uint32_t v = key[j];
+            if ((v & mask) == prefix) {
+                const uint32_t b = (v >> shift) & 255u;
+                atomicAdd(&hcnt[b], 1u);
+                atomicAdd(&hmass[b], (double)__uint_as_float(v));
+            }
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            // the highest bucket at which the running mass reaches the target
+            // (bucket 0 takes whatever is left)
+            double acc = above;
+            uint32_t cacc = cabove;
+            int b = 255;
+            for (; b > 0; --b) {
+                if (hcnt[b] && acc + hmass[b] >= target) break;
+                acc += hmass[b];
+                cacc += hcnt[b];
+            }
+            s_prefix = prefix | ((uint32_t)b << shift);
+            s_above = acc;
+            s_cabove = cacc;
+        }
+        __syncthreads();
+        prefix = s_prefix;
+        above = s_above;
+        cabove = s_cabove;
+        mask |= 255u << shift;
+    }
+    if (threadIdx.x == 0) {
+        const uint32_t ceq = hcnt[prefix & 255u];          // keys equal to T
+        const double T = (double)__uint_as_float(prefix);
+        int64_t m = ceq;                                    // all of them if the target is not met
+        if (T > 0.0 && above + (double)ceq * T >= target) {
+            m = (int64_t)ceil((target - above) / T);
+            m = m < 1 ? 1 : (m > (int64_t)ceq ? (int64_t)ceq : m);
+        }
+        int64_t kk = (int64_t)cabove + m;
+        kk = kk > max_keys ? max_keys : kk;
+        kk_out[h] = (int32_t)(kk > ncand ? ncand : kk);
+    }
+}
+
+// Top-k per KV head: radix select on the score bits, compaction in index
+// order.  kk_head (nullable): a count per head instead of topk (the top-p
+// counts); the output row width stays topk + recent.
+__global__ void __launch_bounds__(kHhTopkThreads)
+k_hh_topk(const float* scores, int32_t n, int32_t topk, const int32_t* kk_head, int32_t recent,
+          int32_t* idx, int32_t* counts) {
     const int h = blockIdx.x;
     const uint32_t* key = reinterpret_cast<const uint32_t*>(scores + (int64_t)h * n);
     const int ncand = max(n - recent, 0);
-    const int kk = min(topk, ncand);
+    const int kk = min(kk_head ? min(kk_head[h], topk) : topk, ncand);
     const int width = topk + recent;
     int32_t* out = idx + (int64_t)h * width;
     __shared__ uint32_t hist[256];
@@ -296,16 +390,20 @@ k_hh_topk(const float* scores, int32_t n, int32_t topk, int32_t recent, int32_t*
     if (threadIdx.x == 0 && counts) counts[h] = kk + nrec;
 }
 
+// Workspace: per-tile and per-row softmax statistics, the scores unless the
+// caller keeps them, then the per-head top-p counts.
 size_t hh_workspace(int32_t n_obs, int32_t n, int32_t hq, int32_t hkv, bool own_scores) {
     const int64_t ntiles = (n + kHhKeys - 1) / kHhKeys;
     size_t b = 2 * (size_t)hq * n_obs * ntiles * 4 + 2 * (size_t)hq * n_obs * 4;
     if (own_scores) b += (size_t)hkv * n * 4;
-    return b + 256;
+    b = (b + 15) & ~size_t(15);
+    return b + (size_t)hkv * 4 + 256;
 }
 
+// top_p > 0: per-head counts from the top-p rule (at most topk) into kk_buf
 template <int D>
-cudaError_t launch_hh(const HhParams& p, int32_t topk, int32_t recent, int32_t* idx,
-                      int32_t* counts, cudaStream_t s) {
+cudaError_t launch_hh(const HhParams& p, int32_t topk, float top_p, int32_t* kk_buf,
+                      int32_t recent, int32_t* idx, int32_t* counts, cudaStream_t s) {
     constexpr int smem = (kHhKeys + kHhRows) * (D + 8) * 2 + 4 * kHhKeys * 4;
     const dim3 grid(p.ntiles, p.hkv);
     k_hh_tile<D, 0><<<grid, 128, smem, s>>>(p);
@@ -314,30 +412,17 @@ cudaError_t launch_hh(const HhParams& p, int32_t topk, int32_t recent, int32_t* 
     const int64_t rows = (int64_t)p.hq * p.n_obs;
     k_hh_rows<<<(unsigned)((rows + 255) / 256), 256, 0, s>>>(p);
     k_hh_tile<D, 1><<<grid, 128, smem, s>>>(p);
-    k_hh_topk<<<p.hkv, kHhTopkThreads, 0, s>>>(p.scores, p.n, topk, recent, idx, counts);
+    if (top_p > 0.f)
+        k_hh_topp_count<<<p.hkv, kHhTopkThreads, 0, s>>>(p.scores, p.n, top_p, topk, recent, kk_buf);
+    k_hh_topk<<<p.hkv, kHhTopkThreads, 0, s>>>(p.scores, p.n, topk, top_p > 0.f ? kk_buf : nullptr,
+                                                recent, idx, counts);
     return cudaGetLastError();
 }
 
-}  // namespace
-
-}  // namespace sp
-
-using namespace sp;
-
-extern "C" sp_status sp_select_workspace_bytes(int32_t n_obs, int32_t n, int32_t num_q_heads,
-                                               int32_t num_kv_heads, size_t* bytes) {
-    if (!bytes) return fail(SP_ERR_INVALID_ARG, "null argument");
-    if (n < 1 || n_obs < 1 || n_obs > n || num_q_heads < 1 || num_kv_heads < 1)
-        return fail(SP_ERR_INVALID_ARG, "need 1 <= n_obs <= n and positive head counts");
-    *bytes = hh_workspace(n_obs, n, num_q_heads, num_kv_heads, true);
-    return SP_OK;
-}
-
-extern "C" sp_status sp_select_heavy_hitters(const void* q_obs, int32_t n_obs, const void* k,
-                                             int32_t n, int32_t num_q_heads, int32_t num_kv_heads,
-                                             int32_t head_dim, int32_t topk, int32_t recent,
-                                             int32_t* idx, int32_t* counts, float* scores,
-                                             void* workspace, size_t workspace_bytes, void* stream) {
+sp_status select_impl(const void* q_obs, int32_t n_obs, const void* k, int32_t n, int32_t num_q_heads,
+                      int32_t num_kv_heads, int32_t head_dim, int32_t topk, float top_p,
+                      int32_t recent, int32_t* idx, int32_t* counts, float* scores, void* workspace,
+                      size_t workspace_bytes, void* stream) {
     if (!q_obs || !k || !idx || !workspace) return fail(SP_ERR_INVALID_ARG, "null argument");
     if (n < 1 || n_obs < 1 || n_obs > n) return fail(SP_ERR_INVALID_ARG, "need 1 <= n_obs <= n");
     if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads)
@@ -369,9 +454,49 @@ extern "C" sp_status sp_select_heavy_hitters(const void* q_obs, int32_t n_obs, c
     p.row_m = reinterpret_cast<float*>(w + 2 * part);
     p.row_l = p.row_m + (size_t)num_q_heads * n_obs;
     p.scores = scores ? scores : p.row_l + (size_t)num_q_heads * n_obs;
+    size_t used = 2 * part + 2 * (size_t)num_q_heads * n_obs * 4 +
+                  (scores ? 0 : (size_t)num_kv_heads * n * 4);
+    used = (used + 15) & ~size_t(15);
+    int32_t* kk_buf = reinterpret_cast<int32_t*>(w + used);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const cudaError_t e = head_dim == 128 ? launch_hh<128>(p, topk, recent, idx, counts, st)
-                                          : launch_hh<64>(p, topk, recent, idx, counts, st);
+    const cudaError_t e =
+        head_dim == 128 ? launch_hh<128>(p, topk, top_p, kk_buf, recent, idx, counts, st)
+                        : launch_hh<64>(p, topk, top_p, kk_buf, recent, idx, counts, st);
     if (e != cudaSuccess) return cuda_fail(e, "selection launch");
     return SP_OK;
+}
+
+}  // namespace
+
+}  // namespace sp
+
+using namespace sp;
+
+extern "C" sp_status sp_select_workspace_bytes(int32_t n_obs, int32_t n, int32_t num_q_heads,
+                                               int32_t num_kv_heads, size_t* bytes) {
+    if (!bytes) return fail(SP_ERR_INVALID_ARG, "null argument");
+    if (n < 1 || n_obs < 1 || n_obs > n || num_q_heads < 1 || num_kv_heads < 1)
+        return fail(SP_ERR_INVALID_ARG, "need 1 <= n_obs <= n and positive head counts");
+    *bytes = hh_workspace(n_obs, n, num_q_heads, num_kv_heads, true);
+    return SP_OK;
+}
+
+extern "C" sp_status sp_select_heavy_hitters(const void* q_obs, int32_t n_obs, const void* k,
+                                             int32_t n, int32_t num_q_heads, int32_t num_kv_heads,
+                                             int32_t head_dim, int32_t topk, int32_t recent,
+                                             int32_t* idx, int32_t* counts, float* scores,
+                                             void* workspace, size_t workspace_bytes, void* stream) {
+    return select_impl(q_obs, n_obs, k, n, num_q_heads, num_kv_heads, head_dim, topk, 0.f, recent,
+                       idx, counts, scores, workspace, workspace_bytes, stream);
+}
+
+extern "C" sp_status sp_select_heavy_hitters_top_p(const void* q_obs, int32_t n_obs, const void* k,
+                                                   int32_t n, int32_t num_q_heads,
+                                                   int32_t num_kv_heads, int32_t head_dim, float top_p,
+                                                   int32_t max_keys, int32_t recent, int32_t* idx,
+                                                   int32_t* counts, float* scores, void* workspace,
+                                                   size_t workspace_bytes, void* stream) {
+    if (!(top_p > 0.f && top_p <= 1.f)) return fail(SP_ERR_INVALID_ARG, "top_p must lie in (0, 1]");
+    return select_impl(q_obs, n_obs, k, n, num_q_heads, num_kv_heads, head_dim, max_keys, top_p,
+                       recent, idx, counts, scores, workspace, workspace_bytes, stream);
 }

@@ -271,6 +271,25 @@ sp_status sp_select_heavy_hitters(const void* q_obs, int32_t n_obs, const void* 
                                   float* scores, void* workspace, size_t workspace_bytes,
                                   void* stream);
 
+/* The "top-p" form of the same selection (runtime article section 2, "the
+ * top-p important tokens"), with the same scores, outputs and workspace:
+ * for head h the candidates j < n - recent are ranked by score (descending;
+ * ties: lower j first) and the shortest prefix whose summed score reaches
+ * top_p times the candidates' total score is kept, at most max_keys keys
+ * (the page budget the caller sizes the RETRIEVAL pages for; none when the
+ * total is 0), then the recent window.  idx rows are max_keys + recent wide.
+ * The sums are taken in float64, so a count whose exact prefix mass lies
+ * within a few float64 roundings of the boundary may come out one higher or
+ * lower than exact arithmetic would give.  SP_ERR_INVALID_ARG unless
+ * 0 < top_p <= 1, as well as for the arguments sp_select_heavy_hitters
+ * refuses. */
+sp_status sp_select_heavy_hitters_top_p(const void* q_obs, int32_t n_obs, const void* k, int32_t n,
+                                        int32_t num_q_heads, int32_t num_kv_heads,
+                                        int32_t head_dim, float top_p, int32_t max_keys,
+                                        int32_t recent, int32_t* idx, int32_t* counts,
+                                        float* scores, void* workspace, size_t workspace_bytes,
+                                        void* stream);
+
 /* Pack / unpack one sequence for a prefill/decode-disaggregated transfer (news
  * summary, "system gains": in the PD-separated setting only the tokens each
  * head keeps travel, up to 6.3x fewer KV bytes).  The summary names no such

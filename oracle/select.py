@@ -10,10 +10,18 @@ softmax probability of j, scale 1/sqrt(d), summed over h's query heads and
 over the observation rows (the last n_obs prompt rows); the selection is the
 topk highest scores among keys below n - recent (ties: lower index first),
 united with the recent window, ascending.
+
+The "top-p" form read from the same sentence: among those candidates, in
+the order (score descending, index ascending), keep the shortest prefix
+whose summed score reaches p times the candidates' total score, at most
+max_keys of them (a page budget), then the recent window.  Sums here are
+exact (rational arithmetic on the given float values, p included: pass the
+float the kernel receives, e.g. a float32 p as np.float32).
 """
 from __future__ import annotations
 
-from typing import List
+from fractions import Fraction
+from typing import List, Set, Tuple
 
 import numpy as np
 
@@ -44,3 +52,39 @@ def select(score_row, n: int, topk: int, recent: int) -> List[int]:
     kk = min(topk, ncand)
     order = sorted(range(ncand), key=lambda j: (-float(score_row[j]), j))[:kk]
     return sorted(order) + list(range(ncand, ncand + min(recent, n)))
+
+
+def top_p_count(score_row, n: int, p: float, max_keys: int, recent: int,
+                rel: float = 1e-9) -> Tuple[int, Set[int]]:
+    """How many candidates the top-p rule keeps for one head, with exact
+    sums: the smallest m such that the m highest-ranked candidates (score
+    descending, index ascending, j < n - recent) hold at least p times the
+    candidates' total score, capped at max_keys (0 when p * total is 0).
+    Also returns every count a float64 evaluation of the same comparison may
+    give: m - 1 (or m + 1) when the exact prefix mass at m - 1 (or m) lies
+    within rel * total of the boundary."""
+    ncand = max(n - recent, 0)
+    vals = [Fraction(float(score_row[j])) for j in range(ncand)]
+    total = sum(vals, Fraction(0))
+    target = Fraction(float(p)) * total
+    if ncand == 0 or target <= 0:
+        return 0, {0}
+    order = sorted(range(ncand), key=lambda j: (-float(score_row[j]), j))
+    prefix = [Fraction(0)]
+    for j in order:
+        prefix.append(prefix[-1] + vals[j])
+    m = next(i for i in range(ncand + 1) if prefix[i] >= target)
+    ok = {m}
+    slack = Fraction(rel) * total
+    if m > 1 and target - prefix[m - 1] <= slack:
+        ok.add(m - 1)
+    if m < ncand and prefix[m] - target <= slack:
+        ok.add(m + 1)
+    return min(m, max_keys), {min(x, max_keys) for x in ok}
+
+
+def select_top_p(score_row, n: int, p: float, max_keys: int, recent: int) -> List[int]:
+    """The top-p selection of one head: the top_p_count highest-ranked
+    candidates, then the recent window; ascending."""
+    m, _ = top_p_count(score_row, n, p, max_keys, recent)
+    return select(score_row, n, m, recent)

@@ -85,3 +85,50 @@ def test_selected_indices_drive_a_retrieval_head():
     ref, lref = oracle.attend(f64(qd), kk, vv, np.array([n]), pt, "f64")
     compare(out, ref, lse, lref, "decode over selected indices")
     assert cache.status() == 0
+
+
+def _check_top_p(q, k, top_p, max_keys, recent, rtol=2e-3):
+    """GPU top-p selection: scores against the oracle's float64 scores; each
+    head's count is the exact rule's count on the GPU's own fp32 scores (or
+    its float64-boundary neighbour), and the kept keys are exactly the
+    highest-ranked ones of that count."""
+    from head_aware_paged_gb300 import sp_select_heavy_hitters_top_p
+    n = k.shape[0]
+    idx, counts, sc = sp_select_heavy_hitters_top_p(q, k, top_p, max_keys, recent, want_scores=True)
+    torch.cuda.synchronize()
+    idx, counts, sc = idx.cpu().numpy(), counts.cpu().numpy(), sc.cpu().numpy()
+    ref = select.scores(f64(q), f64(k))
+    np.testing.assert_allclose(sc, ref, rtol=rtol, atol=1e-6 * ref.max())
+    nrec = min(recent, n)
+    for h in range(k.shape[1]):
+        m, ok = select.top_p_count(sc[h], n, np.float32(top_p), max_keys, recent)
+        got_m = int(counts[h]) - nrec
+        assert got_m in ok, (h, got_m, m, ok)
+        assert idx[h, :counts[h]].tolist() == select.select(sc[h], n, got_m, recent)
+        assert (idx[h, counts[h]:] == -1).all()
+    return counts
+
+
+@pytest.mark.parametrize("d,n,n_obs,hq,hkv", [(64, 1000, 37, 8, 2), (128, 777, 64, 6, 3),
+                                              (128, 4096, 64, 32, 8), (64, 200, 200, 4, 4)])
+def test_top_p_selection(d, n, n_obs, hq, hkv):
+    gpu_ready()
+    q = W.normal((n_obs, hq, d), 11, device="cuda")
+    k = W.normal((n, hkv, d), 12, scale=0.5, device="cuda")
+    for top_p, max_keys, recent in [(0.9, n, 16), (0.5, 64, 0), (0.25, n, 0), (1.0, n, 8),
+                                    (0.999, 50, 3)]:
+        _check_top_p(q, k, top_p, max_keys, recent)
+
+
+def test_top_p_ties_and_arguments():
+    gpu_ready()
+    from head_aware_paged_gb300 import SegPagedError, sp_select_heavy_hitters_top_p
+    d, n = 64, 300
+    q = W.normal((20, 4, d), 3, device="cuda")
+    k = W.normal((n, 2, d), 4, device="cuda")
+    k[100:140] = k[60].clone()                  # equal scores: lower positions first
+    for top_p, max_keys, recent in [(0.3, 400, 0), (0.7, 10, 5), (0.05, 1, 0), (0.6, 0, 20)]:
+        _check_top_p(q, k, top_p, max_keys, recent)
+    for bad in (0.0, -0.5, 1.5, float("nan")):
+        with pytest.raises(SegPagedError):
+            sp_select_heavy_hitters_top_p(q, k, bad, 10, 0)
