@@ -26,7 +26,7 @@ struct Layout {
     size_t pol = 0, npages = 0, seqlen = 0, ptab = 0, idx = 0, fstack = 0, status = 0,
            scales = 0, meta_total = 0;
     size_t tiles = 0, tile_ctr = 0, part_o = 0, part_ml = 0, counters = 0, scratch = 0,
-           ws_total = 0;
+           split_o = 0, split_ml = 0, ws_total = 0;
     int64_t max_tiles = 0, max_parts = 0, max_counter_units = 0, scratch_ints = 0;
     size_t pool_total = 0;
 };
@@ -89,6 +89,8 @@ Layout make_layout(const sp_config* c) {
     L.part_ml = o;  o = align_up(o + L.max_parts * group * 2 * 4, 256);
     L.counters = o; o = align_up(o + L.max_counter_units * 4, 256);
     L.scratch = o;  o = align_up(o + L.scratch_ints * 4, 256);
+    L.split_o = o;  o = align_up(o + (size_t)kPrefillSplitSlots * 2 * 128 * c->head_dim * 4, 256);
+    L.split_ml = o; o = align_up(o + (size_t)kPrefillSplitSlots * 2 * 128 * 2 * 4, 256);
     L.ws_total = o;
     L.pool_total = 2 * (size_t)c->num_pages * c->page_size * c->head_dim *
                    (c->kv_dtype == SP_KV_FP8_E4M3 ? 1 : 2);
@@ -373,6 +375,8 @@ sp_status sp_cache_create(const sp_config* cfg, void* pool, void* meta, void* ws
     c->ws.max_counter_units = L.max_counter_units;
     c->ws.scratch = reinterpret_cast<int32_t*>(wb + L.scratch);
     c->ws.scratch_ints = L.scratch_ints;
+    c->ws.split_o = reinterpret_cast<float*>(wb + L.split_o);
+    c->ws.split_ml = reinterpret_cast<float*>(wb + L.split_ml);
     std::string err;
     const uint64_t rows = (uint64_t)cfg->num_pages * cfg->page_size;
     // bf16: boxes of 64 elements (one 128-byte swizzle row); FP8: a 128-element

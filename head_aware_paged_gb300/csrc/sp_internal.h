@@ -125,6 +125,7 @@ struct Workspace {
     int32_t* tile_ctr;
     float* part_o;        float* part_ml;  int64_t max_parts;
     int32_t* counters;    int64_t max_counter_units;
+    float* split_o;       float* split_ml;        // prefill pieces of split items
     int32_t* scratch;     int64_t scratch_ints;   // export / visible-count staging
 };
 

@@ -165,6 +165,21 @@ SP_HD void cursor_next(const Plan& pl, TileCursor& c) {
     cursor_load(pl, c);
 }
 
+// A cursor on tile t of the plan (0 <= t < pl.ntiles): where a piece of a
+// work item split along its keys starts.
+SP_HD TileCursor cursor_at(const Plan& pl, int64_t t) {
+    TileCursor c;
+    c.s = 0;
+    cursor_load(pl, c);
+    while (c.s < kMaxSegs && t >= c.nt_s) {
+        t -= c.nt_s;
+        c.s += 1;
+        cursor_load(pl, c);
+    }
+    c.t_in = (int32_t)t;
+    return c;
+}
+
 // The tile under the cursor (same result as plan_tile for that index).
 SP_HD KvTile cursor_tile(const TileCursor& c, const UnitPol& u, int32_t i_lo, int32_t i_hi) {
     KvTile k;

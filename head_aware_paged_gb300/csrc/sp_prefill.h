@@ -7,6 +7,10 @@ namespace sp {
 // Upper bound on prefill work items of one call (sizes the workspace list).
 int64_t prefill_max_tiles(const sp_config* c);
 
+// Workspace slots for the pieces of prefill items split along their keys
+// (one slot: unnormalised O and (m, l) of 128 rows of two query tiles).
+constexpr int kPrefillSplitSlots = 256;
+
 // Plan, upload and launch one prefill call (arguments already validated).
 sp_status prefill_impl(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32_t n_seqs,
                        const int32_t* cu_q, const __nv_bfloat16* q, const __nv_bfloat16* k,

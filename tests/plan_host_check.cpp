@@ -61,6 +61,9 @@ static void prefill_case(const UnitPol& u, const int32_t* idx, int P, int64_t n_
         const KvTile kc = cursor_tile(cur, u, (int32_t)i_lo, (int32_t)i_hi);
         cursor_next(pl, cur);
         if (!same_tile(kt, kc)) printf("ERR tile %lld: cursor and index disagree\n", (long long)t);
+        // a cursor placed straight on tile t (where a piece of a split item starts)
+        const KvTile ka = cursor_tile(cursor_at(pl, t), u, (int32_t)i_lo, (int32_t)i_hi);
+        if (!same_tile(kt, ka)) printf("ERR tile %lld: cursor placed on it disagrees\n", (long long)t);
         if (kt.nkeys % 16 != 0 || kt.nkeys > kTileKeys || kt.nvalid < 1 || kt.nvalid > kt.nkeys)
             printf("ERR tile %lld: width %d valid %d\n", (long long)t, kt.nkeys, kt.nvalid);
         if (kt.paged) {

@@ -151,6 +151,48 @@ def test_chunked_ragged_prefill_with_history(P, d, hq, hkv):
     assert cache.status() == 0 and oneshot.status() == 0
 
 
+@pytest.mark.parametrize("P,d,hq,hkv", [(64, 128, 8, 4), (16, 64, 6, 3)])
+def test_long_history_short_chunks_split_items(P, d, hq, hkv):
+    """A few query rows over a long history: every work item is far longer
+    than a CTA's share of the call, so the planner splits each along its key
+    tiles into pieces (up to eight, of at least six tiles) whose partial
+    results the merge kernel combines.  GLOBAL, LOCAL (a ring tile can hold
+    nothing a row sees, so a piece may leave a row empty) and RETRIEVAL heads;
+    chunks of 1, 128 and 200 rows; every row against the oracle."""
+    gpu_ready()
+    rng = np.random.default_rng(5 + d)
+    n_hist, max_len = 9000, 9400
+    pols = []
+    for h in range(hkv):
+        kind = h % 3
+        if kind == G:
+            pols.append(W.HeadPolicy(G))
+        elif kind == L:
+            pols.append(W.HeadPolicy(L, 4, 3000))
+        else:
+            idx = np.sort(rng.choice(np.arange(40, max_len), 1500, replace=False)).astype(np.int32)
+            pols.append(W.HeadPolicy(R, idx=idx))
+    cache = _mk(1, hq, hkv, d, P, 1, max_len + 16, hkv * (max_len // P + 4), max_batch=1,
+                max_tokens=max_len)
+    cache.set_policy(0, to_c_policies([pols]))
+    q = W.normal((max_len, hq, d), 31, device="cuda")
+    k = W.normal((max_len, hkv, d), 32, 0.5, device="cuda")
+    v = W.normal((max_len, hkv, d), 33, device="cuda")
+    cache.build(0, 0, k[:n_hist].contiguous(), v[:n_hist].contiguous())
+    pt = [pol_tuple(p) for p in pols]
+    held = n_hist
+    for c in (1, 128, 200):
+        sl = slice(held, held + c)
+        o, lse = cache.prefill(0, [0], [0, c], q[sl].contiguous(), k[sl].contiguous(),
+                               v[sl].contiguous())
+        ref, lref = oracle.attend(f64(q[sl]), f64(k[:held + c]), f64(v[:held + c]),
+                                  np.arange(held, held + c), pt, "f64", threads=ncores())
+        compare(o, ref, lse, lref, "split items, chunk of %d at %d" % (c, held))
+        cache.append_kv(0, [0], [0, c], k[sl].contiguous(), v[sl].contiguous())
+        held += c
+    assert cache.status() == 0
+
+
 def test_edge_cases():
     """One-row chunks, rows with no visible key (RETRIEVAL before its first
     index: O = 0, LSE = -inf), sink larger than a tile, window 1, odd group."""
