@@ -236,4 +236,39 @@ SP_HD bool key_visible(const KvTile& k, const UnitPol& u, I i, int c, I table_po
 }
 
 
+// Bits [0, n) set, n clamped to [0, 32].
+SP_HD uint32_t low_bits32(int64_t n) {
+    return n <= 0 ? 0u : n >= 32 ? 0xFFFFFFFFu : ((1u << n) - 1u);
+}
+
+// Visibility bits of a paged (history) tile for the query at position i
+// (key c -> bit c % 32 of vm[c / 32]); the unit holds n_b <= i tokens, so
+// every stored position is below i.  GLOBAL and RETRIEVAL slots and LOCAL
+// sink slots are seen by every row: the tile's first nvalid keys.  LOCAL
+// ring slots hold consecutive positions with one break at the ring's newest
+// slot h (newest = n_b - 1 - sink = K * ring_slots + h, see slot_position):
+// A + c up to the break, A - ring_slots + c after it (slots not yet written
+// when K = 0); a row sees those at or after i - window + 1.  Same bits as
+// key_visible on the slots' positions.  Positions and slots fit in 32 bits.
+SP_HD void paged_row_mask(const KvTile& k, const UnitPol& u, int32_t n_b, int32_t i, int P,
+                          uint32_t (&vm)[4]) {
+    const int32_t base = u.sink_pages * P, start = (int32_t)k.start;
+    if (u.kind != kLocal || start < base) {
+        for (int w = 0; w < 4; ++w) vm[w] = low_bits32((int64_t)k.nvalid - 32 * w);
+        return;
+    }
+    const int32_t rs = u.ring * P, q0 = start - base, newest = n_b - 1 - u.sink;
+    const int32_t K = newest / rs, h = newest - K * rs;     // a ring tile exists: newest >= 0
+    const int64_t A = (int64_t)u.sink + (int64_t)K * rs + q0;   // position of key 0, before the break
+    const int64_t lo = (int64_t)i - u.window + 1;                // oldest position the row sees
+    const int64_t brk = min64(max64((int64_t)h - q0 + 1, 0), 128);
+    const int64_t v1 = min64(max64(lo - A, 0), 128);
+    const int64_t v2 = K > 0 ? min64(max64(lo - (A - rs), 0), 128) : 128;
+    for (int w = 0; w < 4; ++w) {
+        const uint32_t before = low_bits32(brk - 32 * w);
+        vm[w] = low_bits32((int64_t)k.nvalid - 32 * w) &
+                ((before & ~low_bits32(v1 - 32 * w)) | (~before & ~low_bits32(v2 - 32 * w)));
+    }
+}
+
 }  // namespace sp

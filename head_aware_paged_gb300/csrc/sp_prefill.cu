@@ -585,7 +585,7 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                     cursor_next(pl, cur);
                     const bool masked = !kt.full;
                     int32_t tpos[4] = {-1, -1, -1, -1};
-                    if (masked && kt.table) {
+                    if (masked && kt.table && !kt.paged) {
                         #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4)
                             tpos[q4] = (int32_t)tile_key_position(kt, it.pol, it.idx, it.n_b,
@@ -612,7 +612,11 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                                      ~lowmask32(i - it.pol.window + 1 - p0 - 32 * w);
                             vm[w] = b;
                         }
+                    } else if (kt.paged) {
+                        // history slots: arithmetic bits (sp_plan.h)
+                        paged_row_mask(kt, it.pol, (int32_t)it.n_b, i, P, vm);
                     } else {
+                        // RETRIEVAL chunk rows: the per-key position table
                         #pragma unroll
                         for (int w = 0; w < 4; ++w) {
                             uint32_t b = 0;
@@ -801,8 +805,8 @@ __global__ void k_prefill_counts(Meta meta, Geo g, int seq, int layer, int h,
     }
 }
 
-// Pieces of split items -> final rows: per (item, query tile) block, one
-// thread per row combines the pieces' (O, m, l): m* = max m, each piece
+// Pieces of split items -> final rows: per (item, query tile, 32 columns)
+// block, one thread per row combines the pieces' (O, m, l): m* = max m, each piece
 // weighted by 2^(m - m*), O = sum w O / sum w l, LSE = m* + log2(sum w l) in
 // natural-log units.  A row no piece saw gives O = 0, LSE = -inf.
 constexpr int kMaxMergeGroups = 1024;
@@ -818,14 +822,16 @@ struct MergeParams {
 
 template <int D>
 __global__ void __launch_bounds__(128) k_prefill_merge(const __grid_constant__ MergeParams p) {
+    // block (group, query tile, 32-column slice); thread = row
     const int4 gr = p.groups[blockIdx.x];
-    const int t = blockIdx.y, r = threadIdx.x;
+    const int t = blockIdx.y, c0 = blockIdx.z * 32, r = threadIdx.x;
     if (r >= gr.z) return;
     const int slot0 = gr.w & 0xFFFF, np = gr.w >> 16;
     float ms[kMaxPieces], wq[kMaxPieces], mx = -INFINITY;
     #pragma unroll
     for (int q = 0; q < kMaxPieces; ++q) {
         ms[q] = -INFINITY;
+        wq[q] = 0.f;
         if (q < np) {
             const float2 ml = p.split_ml[((int64_t)(slot0 + q) * 2 + t) * 128 + r];
             ms[q] = ml.x;
@@ -836,26 +842,33 @@ __global__ void __launch_bounds__(128) k_prefill_merge(const __grid_constant__ M
     float L = 0.f;
     #pragma unroll
     for (int q = 0; q < kMaxPieces; ++q) {
-        const float w = (q < np && ms[q] != -INFINITY) ? exp2f(ms[q] - mx) : 0.f;
-        if (q < np) L += w * wq[q];
+        const float w = ms[q] != -INFINITY ? exp2f(ms[q] - mx) : 0.f;
+        L += w * wq[q];
         wq[q] = w;
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    __nv_bfloat16* orow = p.out + ((int64_t)(gr.x + r) * p.hq + gr.y + t) * D;
-    #pragma unroll 4
-    for (int c4 = 0; c4 < D / 4; c4 += 2) {
-        float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int q = 0; q < np; ++q) {
+    float a[32];
+    #pragma unroll
+    for (int e = 0; e < 32; ++e) a[e] = 0.f;
+    #pragma unroll
+    for (int q = 0; q < kMaxPieces; ++q) {
+        if (q < np) {
             const float4* po = p.split_o + ((int64_t)(slot0 + q) * 2 + t) * (D / 4) * 128 + r;
-            const float4 x = po[c4 * 128], y = po[(c4 + 1) * 128];
-            a[0] += wq[q] * x.x; a[1] += wq[q] * x.y; a[2] += wq[q] * x.z; a[3] += wq[q] * x.w;
-            a[4] += wq[q] * y.x; a[5] += wq[q] * y.y; a[6] += wq[q] * y.z; a[7] += wq[q] * y.w;
+            #pragma unroll
+            for (int e4 = 0; e4 < 8; ++e4) {
+                const float4 x = po[(c0 / 4 + e4) * 128];
+                a[4 * e4] += wq[q] * x.x; a[4 * e4 + 1] += wq[q] * x.y;
+                a[4 * e4 + 2] += wq[q] * x.z; a[4 * e4 + 3] += wq[q] * x.w;
+            }
         }
-        *reinterpret_cast<uint4*>(orow + 4 * c4) =
-            make_uint4(pack_bf16(a[0] * inv, a[1] * inv), pack_bf16(a[2] * inv, a[3] * inv),
-                       pack_bf16(a[4] * inv, a[5] * inv), pack_bf16(a[6] * inv, a[7] * inv));
     }
-    if (p.lse)
+    __nv_bfloat16* orow = p.out + ((int64_t)(gr.x + r) * p.hq + gr.y + t) * D + c0;
+    #pragma unroll
+    for (int e = 0; e < 32; e += 8)
+        *reinterpret_cast<uint4*>(orow + e) =
+            make_uint4(pack_bf16(a[e] * inv, a[e + 1] * inv), pack_bf16(a[e + 2] * inv, a[e + 3] * inv),
+                       pack_bf16(a[e + 4] * inv, a[e + 5] * inv), pack_bf16(a[e + 6] * inv, a[e + 7] * inv));
+    if (p.lse && blockIdx.z == 0)
         p.lse[(int64_t)(gr.x + r) * p.hq + gr.y + t] =
             L > 0.f ? (mx + __log2f(L)) * 0.69314718055994531f : -INFINITY;
 }
@@ -1088,7 +1101,7 @@ sp_status prefill_impl(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32
         mp->out = out;
         mp->lse = lse;
         std::copy(groups.begin(), groups.end(), mp->groups);
-        const dim3 mg((unsigned)groups.size(), (unsigned)p.nq);
+        const dim3 mg((unsigned)groups.size(), (unsigned)p.nq, (unsigned)(D / 32));
         if (D == 128) k_prefill_merge<128><<<mg, 128, 0, stream>>>(*mp);
         else k_prefill_merge<64><<<mg, 128, 0, stream>>>(*mp);
         e = cudaGetLastError();

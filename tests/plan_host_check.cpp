@@ -73,6 +73,21 @@ static void prefill_case(const UnitPol& u, const int32_t* idx, int P, int64_t n_
                 printf("ERR tile %lld: page %lld of %lld owned\n", (long long)t, (long long)last_page,
                        (long long)owned);
         }
+        if (kt.paged) {
+            // the arithmetic row mask of history tiles against the per-key rule
+            for (int64_t r = 0; r < rows; ++r) {
+                uint32_t vm[4];
+                paged_row_mask(kt, u, (int32_t)n_b, (int32_t)(i_lo + r), P, vm);
+                for (int c = 0; c < kTileKeys; ++c) {
+                    const int64_t pos = tile_key_position(kt, u, idx, n_b, c, P);
+                    const bool want = c < kt.nkeys && key_visible<int64_t>(kt, u, i_lo + r, c, pos);
+                    const bool got = (vm[c >> 5] >> (c & 31)) & 1u;
+                    if (want != got)
+                        printf("ERR tile %lld: row mask of key %d (position %lld) for row %lld is %d\n",
+                               (long long)t, c, (long long)pos, (long long)(i_lo + r), (int)got);
+                }
+            }
+        }
         for (int c = 0; c < kt.nkeys; ++c) {
             const int64_t pos = tile_key_position(kt, u, idx, n_b, c, P);
             for (int64_t r = 0; r < rows; ++r) {
