@@ -238,14 +238,13 @@ class PrefillStep:
 
     def run(self, ev_pf=None):
         """One step; ev_pf (optional): a (start, end) event pair per layer
-        recorded around that layer's prefill launch."""
+        that the library records right before and after that layer's
+        prefill kernels (host planning outside the interval)."""
         c = self.cache
         for l in range(self.layers):
             if ev_pf is not None:
-                ev_pf[l][0].record()
+                c.set_launch_events(*ev_pf[l])
             c.prefill(l, [0], [0, self.L], self.q[l], self.k[l], self.v[l], self.out, self.lse)
-            if ev_pf is not None:
-                ev_pf[l][1].record()
             c.append_kv(l, [0], [0, self.L], self.k[l], self.v[l])
         for l in range(self.layers):
             c.append_kv(l, [0], [0, 1], self.k1[l], self.v1[l])
@@ -499,15 +498,14 @@ class DecodeStep:
 
     def run(self, ev_pf=None):
         """One step; ev_pf (optional): a (start, end) event pair per layer
-        recorded around that layer's decode launch."""
+        that the library records right before and after that layer's
+        decode kernel (host planning outside the interval)."""
         c = self.cache
         for l in range(self.layers):
             c.append_kv(l, self.seqs, self.cu, self.kn, self.vn)
             if ev_pf is not None:
-                ev_pf[l][0].record()
+                c.set_launch_events(*ev_pf[l])
             c.decode(l, self.seqs, self.qs, self.out, self.lse)
-            if ev_pf is not None:
-                ev_pf[l][1].record()
         self.t += 1
 
 
@@ -580,6 +578,11 @@ def timed_steps(st, steps, warmup, ws, rank, decode):
     E = lambda: torch.cuda.Event(enable_timing=True)
     ev = [(E(), E()) for _ in range(steps)]
     evk = [[(E(), E()) for _ in range(st.layers)] for _ in range(steps)]
+    for row in evk:                 # the library records these: create them first
+        for pair in row:
+            for e in pair:
+                e.record()
+    torch.cuda.synchronize()
     work, kern_work = [], []
     clocks = ClockSampler(gpu_uuid() if rank == 0 else None)
     if rank == 0:

@@ -282,6 +282,21 @@ def sp_selftest_bounded_wait(handle, limit_cycles: int, mode: int, stream=None) 
     check(load().sp_selftest_bounded_wait(handle, limit_cycles, mode, _stream(stream)))
 
 
+def sp_set_launch_events(handle, start=None, end=None) -> None:
+    """Arm two torch.cuda.Event objects for the next attention call on the
+    cache: it records `start` right before its first kernel and `end` right
+    after its last (see the C header); no events disarm.  Each event must
+    have been recorded once already, so that its CUDA event exists."""
+    def raw(e):
+        if e is None:
+            return c_void_p(0)
+        h = int(e.cuda_event)
+        if h == 0:
+            raise ValueError("record the event once before arming it")
+        return c_void_p(h)
+    check(load().sp_set_launch_events(handle, raw(start), raw(end)))
+
+
 def sp_last_error() -> str:
     return load().sp_last_error().decode(errors="replace")
 
@@ -414,3 +429,8 @@ class SegPagedCache:
 
     def status(self, stream=None) -> int:
         return sp_get_status(self.handle, stream)
+
+    def set_launch_events(self, start=None, end=None) -> None:
+        """Time the next attention call's kernels with two recorded-once
+        torch.cuda.Event objects (sp_set_launch_events)."""
+        sp_set_launch_events(self.handle, start, end)

@@ -26,7 +26,8 @@ EXPORTS = ("sp_required_bytes", "sp_cache_create", "sp_cache_destroy", "sp_set_p
            "sp_select_heavy_hitters_top_p", "sp_set_kv_scales",
            "sp_release_seq", "sp_export_table", "sp_visible_count", "sp_seq_len",
            "sp_free_pages", "sp_count_prefill_pairs", "sp_count_decode_bytes",
-           "sp_get_status", "sp_selftest_bounded_wait", "sp_last_error")
+           "sp_get_status", "sp_selftest_bounded_wait", "sp_set_launch_events",
+           "sp_last_error")
 
 
 class SegPagedError(RuntimeError):
@@ -90,6 +91,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "sp_count_decode_bytes": [P, c_int32, I32P, c_int32, I64P, I64P],
         "sp_get_status": [P, P, I32P],
         "sp_selftest_bounded_wait": [P, c_int64, c_int32, P],
+        "sp_set_launch_events": [P, P, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)

@@ -612,8 +612,19 @@ sp_status sp_attention_decode(sp_cache* c, int32_t layer, const int32_t* seq_ids
     p->part_ml = c->ws.part_ml;
     p->counters = c->ws.counters;
     p->scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c->cfg.head_dim));
+    launch_mark_start(c, static_cast<cudaStream_t>(stream));
     cudaError_t e = launch_decode(c, *p, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    launch_mark_end(c, static_cast<cudaStream_t>(stream));
+    return SP_OK;
+}
+
+sp_status sp_set_launch_events(sp_cache* c, void* start_event, void* end_event) {
+    if (!c) return fail(SP_ERR_INVALID_ARG, "null handle");
+    if ((start_event == nullptr) != (end_event == nullptr))
+        return fail(SP_ERR_INVALID_ARG, "give both events or neither");
+    c->launch_ev[0] = static_cast<cudaEvent_t>(start_event);
+    c->launch_ev[1] = static_cast<cudaEvent_t>(end_event);
     return SP_OK;
 }
 

@@ -120,7 +120,9 @@ extern "C" sp_status sp_attention_decode_static_scratch(sp_cache* c, int32_t lay
     // the merge tickets must start at zero in every call
     e = cudaMemsetAsync(p.counters, 0, (size_t)n_units * sizeof(int32_t), st);
     if (e != cudaSuccess) return cuda_fail(e, "clearing the decode tickets");
+    launch_mark_start(c, st);
     e = launch_decode(c, p, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    launch_mark_end(c, st);
     return SP_OK;
 }

@@ -160,6 +160,9 @@ struct sp_cache {
     size_t stage_bytes = 0;                       // size of each buffer
     int stage_next = 0;
     bool prefill_checked[3][4] = {};             // [FP8 ? 2 : D == 128][log2(P) - 4]: attributes set
+    // Caller's event pair armed by sp_set_launch_events for the next
+    // attention call (both null when not armed).
+    cudaEvent_t launch_ev[2] = {};
     ~sp_cache();
 };
 
@@ -176,6 +179,17 @@ cudaError_t stage_copy(sp_cache* c, int slot, void* dst, size_t bytes, cudaStrea
 // none listed twice.
 bool valid_layer(const sp_cache* c, int32_t layer);
 sp_status check_seq_list(const sp_cache* c, const int32_t* seq_ids, int32_t n_seqs);
+
+// Armed launch events (sp_set_launch_events): the start is recorded right
+// before an attention call's first kernel, the end right after its last,
+// which also disarms the pair.
+inline void launch_mark_start(sp_cache* c, cudaStream_t s) {
+    if (c->launch_ev[0]) cudaEventRecord(c->launch_ev[0], s);
+}
+inline void launch_mark_end(sp_cache* c, cudaStream_t s) {
+    if (c->launch_ev[1]) cudaEventRecord(c->launch_ev[1], s);
+    c->launch_ev[0] = c->launch_ev[1] = nullptr;
+}
 
 // Error plumbing (sp_api.cu).
 sp_status fail(sp_status s, const std::string& msg);

@@ -36,7 +36,7 @@
 #include <climits>
 #include <cmath>
 #include <memory>
-#include <queue>
+#include <functional>
 #include <utility>
 #include <vector>
 
@@ -922,6 +922,11 @@ sp_status prefill_impl(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32
     p.split_ml = reinterpret_cast<float2*>(c->ws.split_ml);
     struct Cand { int64_t cost; int32_t unit; int4 item; };   // unit: call sequence * Hkv + KV head
     std::vector<Cand> whole;
+    {
+        size_t n_rb = 0;
+        for (int b = 0; b < n_seqs; ++b) n_rb += (size_t)(cu_q[b + 1] - cu_q[b] + 127) / 128;
+        whole.reserve(n_rb * c->cfg.num_kv_heads * pairs);
+    }
     const int P = c->cfg.page_size;
     for (int b = 0; b < n_seqs; ++b) {
         const int seq = seq_ids[b];
@@ -963,6 +968,7 @@ sp_status prefill_impl(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32
     for (const Cand& cd : whole) total += cd.cost;
     const double share = (double)total / std::max(1, c->num_sms);
     std::vector<Cand> cands;
+    cands.reserve(whole.size() + kPrefillSplitSlots);
     std::vector<int4> groups;                  // merge: {row_base, first head, rows, slot | pieces << 16}
     int slots = 0;
     for (const Cand& cd : whole) {
@@ -1014,43 +1020,63 @@ sp_status prefill_impl(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32
                          [&](int32_t a, int32_t b2) { return unit_cost[a] > unit_cost[b2]; });
         for (int r = 0; r < n_units; ++r) rank[by_cost[r]] = r;
     }
-    std::stable_sort(cands.begin(), cands.end(), [&](const Cand& a, const Cand& b2) {
-        return rank[a.unit] != rank[b2.unit] ? rank[a.unit] < rank[b2.unit] : a.cost > b2.cost;
-    });
+    // One sort of packed keys (unit rank, cost descending, candidate index:
+    // a stable order); a comparison sort of the records when a field would
+    // not fit its bits.
+    const size_t n_items = cands.size();
+    std::vector<uint32_t> order(n_items);
+    if (n_units < (1 << 16) && n_items < (size_t(1) << 20)) {
+        // cost = kTileCost * tiles + kItemCost < 2^28 for tiles < 2^20
+        std::vector<uint64_t> key(n_items);
+        for (size_t i = 0; i < n_items; ++i)
+            key[i] = ((uint64_t)rank[cands[i].unit] << 48) |
+                     ((uint64_t)((int64_t(1) << 28) - 1 - cands[i].cost) << 20) | (uint64_t)i;
+        std::sort(key.begin(), key.end());
+        for (size_t i = 0; i < n_items; ++i) order[i] = (uint32_t)(key[i] & 0xFFFFFu);
+    } else {
+        for (size_t i = 0; i < n_items; ++i) order[i] = (uint32_t)i;
+        std::stable_sort(order.begin(), order.end(), [&](uint32_t a, uint32_t b2) {
+            const Cand &x = cands[a], &y = cands[b2];
+            return rank[x.unit] != rank[y.unit] ? rank[x.unit] < rank[y.unit] : x.cost > y.cost;
+        });
+    }
     // Greedy assignment in that order: each item goes to the CTA with the
-    // least work so far (longest-processing-time rule within a unit).
-    const int grid = (int)std::min<int64_t>(c->num_sms, (int64_t)cands.size());
-    std::vector<int64_t> load(grid, 0);
-    std::vector<std::vector<int4>> per(grid);
+    // least work so far (longest-processing-time rule within a unit; ties to
+    // the lower CTA).
+    const int grid = (int)std::min<int64_t>(c->num_sms, (int64_t)n_items);
+    std::vector<int32_t> owner(n_items);
+    std::vector<int32_t> fill(grid + 1, 0);
     {
         typedef std::pair<int64_t, int> LoadCta;
-        std::priority_queue<LoadCta, std::vector<LoadCta>, std::greater<LoadCta>> heap;
-        for (int g2 = 0; g2 < grid; ++g2) heap.push(LoadCta(0, g2));
-        for (const Cand& cd : cands) {
-            LoadCta top = heap.top();
-            heap.pop();
-            per[top.second].push_back(cd.item);
-            top.first += cd.cost;
-            heap.push(top);
+        std::vector<LoadCta> heap(grid);
+        for (int g2 = 0; g2 < grid; ++g2) heap[g2] = LoadCta(0, g2);   // a valid min-heap
+        const auto later = std::greater<LoadCta>();
+        for (size_t k2 = 0; k2 < n_items; ++k2) {
+            const uint32_t i = order[k2];
+            std::pop_heap(heap.begin(), heap.end(), later);
+            LoadCta& top = heap.back();
+            owner[i] = top.second;
+            ++fill[top.second + 1];
+            top.first += cands[i].cost;
+            std::push_heap(heap.begin(), heap.end(), later);
         }
     }
-    // The items grouped by CTA, then the CTA offsets: inside the kernel
-    // parameters when they fit, else one upload through the next pinned
-    // staging buffer (asynchronous; waits only if that buffer's previous
-    // copy has not run yet)
-    const size_t n_items = cands.size();
+    // The items grouped by CTA (each CTA's in the sorted order), then the CTA
+    // offsets: inside the kernel parameters when they fit, else one upload
+    // through the next pinned staging buffer (asynchronous; waits only if
+    // that buffer's previous copy has not run yet)
     const size_t words = n_items + (grid + 1 + 3) / 4;
     const bool inl = words <= (size_t)kInlineWords;
     int si = -1;
     int4* buf = inl ? p.inl : static_cast<int4*>(stage_acquire(c, words * sizeof(int4), &si));
     if (!buf) return fail(SP_ERR_CUDA, "prefill staging buffer");
     int32_t* off = reinterpret_cast<int32_t*>(buf + n_items);
-    size_t pos = 0;
-    for (int g2 = 0; g2 < grid; ++g2) {
-        off[g2] = (int32_t)pos;
-        for (const int4& it : per[g2]) buf[pos++] = it;
+    for (int g2 = 0; g2 < grid; ++g2) fill[g2 + 1] += fill[g2];
+    for (int g2 = 0; g2 <= grid; ++g2) off[g2] = fill[g2];
+    for (size_t k2 = 0; k2 < n_items; ++k2) {
+        const uint32_t i = order[k2];
+        buf[fill[owner[i]]++] = cands[i].item;
     }
-    off[grid] = (int32_t)pos;
     p.n_items = (int32_t)n_items;
     p.inline_words = inl ? (int32_t)words : 0;
     cudaError_t e = cudaSuccess;
@@ -1070,6 +1096,7 @@ sp_status prefill_impl(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32
         !encode_tmap_2d(&tv, v, (uint64_t)c->cfg.num_kv_heads * D, T,
                         (uint64_t)c->cfg.num_kv_heads * D * 2, 64, 128, true, &err))
         return fail(SP_ERR_CUDA, err);
+    launch_mark_start(c, stream);
 #define SP_PF(DD, PP) \
     if (D == DD && P == PP) e = launch_prefill_t<DD, PP>(c, p, grid, tq, tk, tv, stream); else
 #define SP_PF8(PP) \
@@ -1100,6 +1127,7 @@ sp_status prefill_impl(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32
         e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "prefill merge launch");
     }
+    launch_mark_end(c, stream);
     return SP_OK;
 }
 

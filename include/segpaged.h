@@ -374,6 +374,22 @@ sp_status sp_get_status(sp_cache* cache, void* stream, int32_t* word);
 sp_status sp_selftest_bounded_wait(sp_cache* cache, int64_t limit_cycles, int32_t mode,
                                    void* stream);
 
+/* Instrumentation for profilers and benchmarks (the pages have no
+ * counterpart).  Arms one pair of caller-created CUDA events (cudaEvent_t
+ * handles passed as void*) for the next attention call on this cache
+ * (sp_attention_prefill, sp_attention_decode or
+ * sp_attention_decode_static_scratch): that call records start_event on its
+ * stream immediately before its first kernel launch and end_event
+ * immediately after its last one (the prefill's merge included), so the
+ * interval between them is the device time of the call's kernels without
+ * the host's planning, which otherwise shows in events recorded around the
+ * call whenever the device is idle while the host plans.  The pair is used
+ * by one call and then disarmed (a call that fails may leave it armed).
+ * Both null disarms.  The events stay owned by the caller and
+ * must stay alive until that call has been made.
+ * SP_ERR_INVALID_ARG for a null cache or exactly one null event. */
+sp_status sp_set_launch_events(sp_cache* cache, void* start_event, void* end_event);
+
 /* Message of the last failing call on this thread ("" if none). */
 const char* sp_last_error(void);
 
