@@ -53,6 +53,7 @@ namespace {
 constexpr int kPfThreads = 384;        // 3 warpgroups: 2 softmax, 1 producer/MMA
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp2 = 10;          // second MMA issuer (bf16 pages, two query tiles)
 // Register split between the warpgroups (setmaxnreg).  The block is launched
 // with kLaunchRegs per thread (384 threads x 168 = 64512 of the SM's 65536);
 // the producer/MMA warpgroup drops to kLowRegs and each softmax warpgroup
@@ -66,6 +67,7 @@ constexpr int kSmemLimit = 232448;     // 227 KB per CTA
 constexpr int kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;   // lazy-rescale threshold (log2 units)
 constexpr int kPrefetchTiles = 3;      // K/V tiles brought into L2 ahead of their loads
+constexpr int64_t kTwoIssuerTilesPerItem = 32;   // two MMA issuers up to this mean item length
 constexpr int64_t kTileCost = 160;     // work-assignment cost of one K/V tile
 constexpr int64_t kItemCost = 480;     // and of one work item's fixed part
 constexpr int kMinPieceTiles = 6;      // key tiles of a piece of a split item, at least
@@ -194,7 +196,7 @@ __device__ __forceinline__ uint32_t lowmask32(int32_t n) {
     return n <= 0 ? 0u : n >= 32 ? 0xFFFFFFFFu : ((1u << n) - 1u);
 }
 
-template <int D, int P, bool F8>
+template <int D, int P, bool F8, bool TWO = false>
 __global__ void __launch_bounds__(kPfThreads, 1)
 k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tmQ,
           const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -219,7 +221,10 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
     uint64_t* mma_done = o_empty + 2;
     uint64_t* f_full = mma_done + 1;                  // [2] FP8 code slot landed
     uint64_t* f_empty = f_full + 2;                   // [2] FP8 code slot converted
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(f_empty + 2);
+    // turn tokens of the two MMA issuers: issuer t arrives on tok[t] after
+    // each block it issued
+    uint64_t* tok = f_empty + 2;                      // [2]
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tok + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     // MMA width (keys) of the tile each K/V stage holds, written by the
     // producer before the stage's copies; read by the MMA thread after the
@@ -240,19 +245,28 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
     // space; no __ldg there) or in the workspace
     const int4* items = p.inline_words ? p.inl : p.items;
     const int32_t* cta_off = p.inline_words ? reinterpret_cast<const int32_t*>(p.inl + p.n_items) : p.cta_off;
+    // TWO (calls of short items, two query tiles, bf16 K/V; the host's
+    // choice): one MMA-issuing thread per query tile (warps 9 and 10), taking
+    // turns block by block.  A separate instance, so that the one-issuer
+    // kernel keeps its code size.
+    static_assert(!(TWO && F8), "FP8 history keeps warp 10 for the code conversion");
+    constexpr bool two = TWO;
+    constexpr uint32_t nissue = TWO ? 2u : 1u;
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        mbar_init(q_empty, 1);
-        for (int s = 0; s < NS; ++s) { mbar_init(&kv_full[s], 1); mbar_init(&kv_empty[s], 1); }
+        mbar_init(q_empty, nissue);          // released by every issuer's last QK
+        for (int s = 0; s < NS; ++s) { mbar_init(&kv_full[s], 1); mbar_init(&kv_empty[s], nissue); }
         for (int t = 0; t < 2; ++t) {
             mbar_init(&s_full[t], 1);
             mbar_init(&p_full[t], 4);          // one arrival per softmax warp
             mbar_init(&o_full[t], 1);
             mbar_init(&o_empty[t], 4);
         }
-        mbar_init(mma_done, 1);
+        mbar_init(mma_done, nissue);
         for (int f = 0; f < 2; ++f) { mbar_init(&f_full[f], 1); mbar_init(&f_empty[f], 1); }
+        mbar_init(&tok[0], 1);
+        mbar_init(&tok[1], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -374,7 +388,7 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
         for (uint32_t s = 0; s < NS && s < L; ++s)
             mbar_wait(&kv_full[s], ((L - 1 - s) / NS) & 1, nullptr, nullptr);
         if (q_loads > 0) mbar_wait(q_full, (q_loads - 1) & 1, nullptr, nullptr);
-      } else if (warp == kMmaWarp && lane == 0) {
+      } else if (lane == 0 && (warp == kMmaWarp || (two && warp == kMmaWarp2))) {
         // ------------------------------ MMA issuer ------------------------------
         const uint32_t q_addr = smem_u32(sQ), kv_addr = smem_u32(sKV);
         const uint32_t idesc_pv = idesc_bf16(128, D, true);
@@ -431,6 +445,77 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
         uint32_t q_uses = 0, L = 0, e = 0, tiles = 0;   // both query tiles see every K/V tile
         bool ok = true;
         const int n_end = cta_off[cta + 1];
+        if constexpr (TWO) {
+        // One issuer per query tile.  The CTA's blocks (a tile's QK of an
+        // item's first K tile, then per K/V tile its PV + next QK) alternate
+        // between the issuers, tile 0 first: each issues its block only after
+        // the other has issued the one before (tokens), so the tensor pipe
+        // never interleaves the two tiles' MMAs, while each issuer waits for
+        // its own P, stages and tokens as the other's block runs.  Stages and
+        // the Q buffer are released when both issuers have committed.
+        const int t = warp - kMmaWarp;
+        uint32_t nb = 0;                               // blocks this issuer issued
+        auto take_turn = [&]() -> bool {
+            if (t == 0) return nb == 0 || mbar_wait(&tok[1], (nb - 1) & 1, abort_flag, status);
+            return mbar_wait(&tok[0], nb & 1, abort_flag, status);
+        };
+        auto pass_turn = [&]() { mbar_arrive(&tok[t]); ++nb; };
+        for (int n = cta_off[cta]; n < n_end && ok; ++n) {
+            const int nt = items[n].w & 0xFFFFF;
+            if (nt == 0) continue;
+            if (!mbar_wait(q_full, q_uses & 1, abort_flag, status)) { ok = false; break; }
+            ++q_uses;
+            const uint32_t stK = L % NS;
+            if (!mbar_wait(&kv_full[stK], (L / NS) & 1, abort_flag, status)) { ok = false; break; }
+            ++L;
+            const int nk0 = stage_keys[stK];
+            tc_fence_after();
+            if (!take_turn()) { ok = false; break; }
+            issue_qk(t, stK, nk0);
+            tc_commit(&s_full[t]);
+            pass_turn();
+            tc_commit(&kv_empty[stK]);
+            if (nt == 1) tc_commit(q_empty);
+            for (int j = 0; j < nt && ok; ++j) {
+                const uint32_t stV = L % NS;
+                if (!mbar_wait(&kv_full[stV], (L / NS) & 1, abort_flag, status)) { ok = false; break; }
+                ++L;
+                const int nkv = stage_keys[stV];
+                const bool more = j + 1 < nt;
+                uint32_t stK2 = 0;
+                int nk2 = 0;
+                if (more) {
+                    stK2 = L % NS;
+                    if (!mbar_wait(&kv_full[stK2], (L / NS) & 1, abort_flag, status)) { ok = false; break; }
+                    ++L;
+                    nk2 = stage_keys[stK2];
+                }
+                const bool first = j == 0 && e > 0;     // O_t still holds the last item
+                if (!mbar_wait(&p_full[t], tiles & 1, abort_flag, status)) { ok = false; break; }
+                if (first && !mbar_wait(&o_empty[t], (e - 1) & 1, abort_flag, status)) { ok = false; break; }
+                tc_fence_after();
+                if (!take_turn()) { ok = false; break; }
+                if (nkv == 128 && more) {
+                    issue_pv_full(t, stV, j > 0);
+                    tc_commit(&o_full[t]);
+                    issue_qk(t, stK2, nk2);
+                    tc_commit(&s_full[t]);
+                } else {
+                    issue_pv(t, stV, nkv, j > 0);
+                    tc_commit(&o_full[t]);
+                    if (more) { issue_qk(t, stK2, nk2); tc_commit(&s_full[t]); }
+                }
+                pass_turn();
+                ++tiles;
+                tc_commit(&kv_empty[stV]);
+                if (more) {
+                    tc_commit(&kv_empty[stK2]);
+                    if (j + 2 == nt) tc_commit(q_empty);
+                }
+            }
+            ++e;
+        }
+        } else {
         for (int n = cta_off[cta]; n < n_end && ok; ++n) {
             const int nt = items[n].w & 0xFFFFF;
             if (nt == 0) continue;
@@ -489,6 +574,7 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                 }
             }
             ++e;
+        }
         }
         // all MMAs issued by this thread complete before TMEM can be freed
         tc_commit(mma_done);
@@ -873,24 +959,24 @@ static_assert(sizeof(MergeParams) <= 32764, "merge parameters exceed the kernel 
 static_assert(sizeof(PrefillParams) + 5 * sizeof(CUtensorMap) <= 32764,
               "prefill parameters exceed the kernel parameter space");
 
-template <int D, int P, bool F8 = false>
+template <int D, int P, bool F8 = false, bool TWO = false>
 cudaError_t launch_prefill_t(sp_cache* c, const PrefillParams& p, int grid,
                              const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                              cudaStream_t s) {
     using Sh = PfShape<D, F8>;
-    bool& checked = c->prefill_checked[F8 ? 2 : D == 128][P == 16 ? 0 : P == 32 ? 1 : P == 64 ? 2 : 3];
+    bool& checked = c->prefill_checked[TWO ? 3 : F8 ? 2 : D == 128][P == 16 ? 0 : P == 32 ? 1 : P == 64 ? 2 : 3];
     if (!checked) {   // once per cache and kernel instance
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, k_prefill<D, P, F8>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, k_prefill<D, P, F8, TWO>);
         if (e != cudaSuccess) return e;
         // The setmaxnreg split assumes exactly kLaunchRegs registers per thread
         // at launch; anything else could leave an increase waiting forever.
         if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(k_prefill<D, P, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmem);
+        e = cudaFuncSetAttribute(k_prefill<D, P, F8, TWO>, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmem);
         if (e != cudaSuccess) return e;
         checked = true;
     }
-    k_prefill<D, P, F8><<<grid, kPfThreads, Sh::kSmem, s>>>(p, tq, tk, tv, c->tm_kpool, c->tm_vpool);
+    k_prefill<D, P, F8, TWO><<<grid, kPfThreads, Sh::kSmem, s>>>(p, tq, tk, tv, c->tm_kpool, c->tm_vpool);
     return cudaGetLastError();
 }
 
@@ -1079,6 +1165,17 @@ sp_status prefill_impl(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32
     }
     p.n_items = (int32_t)n_items;
     p.inline_words = inl ? (int32_t)words : 0;
+    // Two MMA issuers (one per query tile) save most of an item boundary's
+    // hand-over, where one issuer sits behind its own commits and waits while
+    // the other tile's P is ready, but their block-by-block turn-taking costs
+    // a little on every block: measured +7 % on 8K-token calls (about 12
+    // tiles an item), −3 % on 128K-token calls (about 120).
+    bool two = false;
+    if (!c->geo.fp8 && p.nq == 2 && c->cfg.head_dim == 128) {
+        int64_t tiles_total = 0;
+        for (const Cand& cd : cands) tiles_total += cd.item.w & 0xFFFFF;
+        two = n_items > 0 && tiles_total <= kTwoIssuerTilesPerItem * (int64_t)n_items;
+    }
     cudaError_t e = cudaSuccess;
     if (!inl) {
         p.items = c->ws.tiles;
@@ -1099,10 +1196,15 @@ sp_status prefill_impl(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32
     launch_mark_start(c, stream);
 #define SP_PF(DD, PP) \
     if (D == DD && P == PP) e = launch_prefill_t<DD, PP>(c, p, grid, tq, tk, tv, stream); else
+#define SP_PF2(PP) \
+    if (P == PP) e = launch_prefill_t<128, PP, false, true>(c, p, grid, tq, tk, tv, stream); else
 #define SP_PF8(PP) \
     if (D == 128 && P == PP) e = launch_prefill_t<128, PP, true>(c, p, grid, tq, tk, tv, stream); else
     if (c->geo.fp8) {   // FP8 pages (head_dim 128, checked at create)
         SP_PF8(16) SP_PF8(32) SP_PF8(64) SP_PF8(128)
+        e = cudaErrorInvalidValue;
+    } else if (two) {   // head_dim 128, two query tiles, short items
+        SP_PF2(16) SP_PF2(32) SP_PF2(64) SP_PF2(128)
         e = cudaErrorInvalidValue;
     } else {
         SP_PF(64, 16) SP_PF(64, 32) SP_PF(64, 64) SP_PF(64, 128)
@@ -1110,6 +1212,7 @@ sp_status prefill_impl(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32
         e = cudaErrorInvalidValue;
     }
 #undef SP_PF
+#undef SP_PF2
 #undef SP_PF8
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     if (!groups.empty()) {
