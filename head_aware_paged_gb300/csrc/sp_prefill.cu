@@ -24,6 +24,8 @@
 //                grew by more than 2^8 (lazy rescale).
 //   The two query tiles share every K/V tile and ping-pong on the tensor core:
 //   while one softmax group works, the MMA warp runs the other's PV and next QK.
+//   With bf16 K/V and head_dim 128 each query tile has its own issuing thread
+//   (warps 9 and 10) and the two take turns block by block.
 // Work items are assigned to CTAs on the host, longest first, each to the
 // CTA with the least work so far (greedy), so no SM idles at the tail; when
 // the call's K/V exceeds about half of L2, one (sequence, KV head) unit after
@@ -67,7 +69,10 @@ constexpr int kSmemLimit = 232448;     // 227 KB per CTA
 constexpr int kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;   // lazy-rescale threshold (log2 units)
 constexpr int kPrefetchTiles = 3;      // K/V tiles brought into L2 ahead of their loads
-constexpr int64_t kTwoIssuerTilesPerItem = 32;   // two MMA issuers up to this mean item length
+// Two MMA issuers: the turn passes this many MMAs before the end of a block
+// (1, 2 and 3 measured within 1 % of each other; at the very end, the hand-over
+// left the tensor pipe idle: 0.67 instead of 0.73 of peak on 128K calls).
+constexpr int kTurnEarly = 2;
 constexpr int64_t kTileCost = 160;     // work-assignment cost of one K/V tile
 constexpr int64_t kItemCost = 480;     // and of one work item's fixed part
 constexpr int kMinPieceTiles = 6;      // key tiles of a piece of a split item, at least
@@ -245,10 +250,10 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
     // space; no __ldg there) or in the workspace
     const int4* items = p.inline_words ? p.inl : p.items;
     const int32_t* cta_off = p.inline_words ? reinterpret_cast<const int32_t*>(p.inl + p.n_items) : p.cta_off;
-    // TWO (calls of short items, two query tiles, bf16 K/V; the host's
-    // choice): one MMA-issuing thread per query tile (warps 9 and 10), taking
-    // turns block by block.  A separate instance, so that the one-issuer
-    // kernel keeps its code size.
+    // TWO (two query tiles, bf16 K/V, head_dim 128; the host's choice): one
+    // MMA-issuing thread per query tile (warps 9 and 10), taking turns block
+    // by block.  A separate instance: the one-issuer kernel (FP8 history,
+    // one query tile, head_dim 64) keeps its code size.
     static_assert(!(TWO && F8), "FP8 history keeps warp 10 for the code conversion");
     constexpr bool two = TWO;
     constexpr uint32_t nissue = TWO ? 2u : 1u;
@@ -412,6 +417,20 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                 tc_mma_acc(d, a0 + off, kmaj_hi, b0 + off, kmaj_hi, idesc);
             }
         };
+        // The same QK with `before_last` run kTurnEarly MMAs before its end.
+        auto issue_qk_hook = [&](int t, uint32_t st, int nkeys, auto&& before_last) {
+            const uint32_t idesc = idesc_bf16(128, nkeys, false);
+            const uint32_t a0 = q_lo + ((t * S::kQBytes) >> 4);
+            const uint32_t b0 = k_lo + ((st * S::kKVBytes) >> 4);
+            const uint32_t d = tmem + t * 128;
+            tc_mma_first(d, a0, kmaj_hi, b0, kmaj_hi, idesc);
+            #pragma unroll
+            for (int ks = 1; ks < D / 16; ++ks) {
+                const uint32_t off = ((ks >> 2) * S::kHalfBytes + (ks & 3) * 32) >> 4;
+                if (ks == D / 16 - kTurnEarly) before_last();
+                tc_mma_acc(d, a0 + off, kmaj_hi, b0 + off, kmaj_hi, idesc);
+            }
+        };
         // O_t (+)= P_t V: P_t sits in TMEM over the first 64 columns of S_t
         // (16 keys = 8 columns per K step), V from shared memory.  The tensor
         // core runs this thread's MMAs in issue order, so S_t of the next tile
@@ -448,11 +467,13 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
         if constexpr (TWO) {
         // One issuer per query tile.  The CTA's blocks (a tile's QK of an
         // item's first K tile, then per K/V tile its PV + next QK) alternate
-        // between the issuers, tile 0 first: each issues its block only after
-        // the other has issued the one before (tokens), so the tensor pipe
-        // never interleaves the two tiles' MMAs, while each issuer waits for
-        // its own P, stages and tokens as the other's block runs.  Stages and
-        // the Q buffer are released when both issuers have committed.
+        // between the issuers, tile 0 first: each starts its block only after
+        // the other has issued all but the last kTurnEarly MMAs of the block
+        // before (tokens), so the two tiles' MMAs meet in the tensor pipe only
+        // at a block's tail and the pipe does not run dry at the hand-over,
+        // while each issuer does its own commits and waits for its P and
+        // stages as the other's block runs.  Stages and the Q buffer are
+        // released when both issuers have committed.
         const int t = warp - kMmaWarp;
         uint32_t nb = 0;                               // blocks this issuer issued
         auto take_turn = [&]() -> bool {
@@ -471,9 +492,8 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
             const int nk0 = stage_keys[stK];
             tc_fence_after();
             if (!take_turn()) { ok = false; break; }
-            issue_qk(t, stK, nk0);
+            issue_qk_hook(t, stK, nk0, pass_turn);
             tc_commit(&s_full[t]);
-            pass_turn();
             tc_commit(&kv_empty[stK]);
             if (nt == 1) tc_commit(q_empty);
             for (int j = 0; j < nt && ok; ++j) {
@@ -495,17 +515,23 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                 if (first && !mbar_wait(&o_empty[t], (e - 1) & 1, abort_flag, status)) { ok = false; break; }
                 tc_fence_after();
                 if (!take_turn()) { ok = false; break; }
+                // the turn passes two MMAs before the block's end, so the
+                // other issuer's first MMAs queue while this one's last run
                 if (nkv == 128 && more) {
                     issue_pv_full(t, stV, j > 0);
                     tc_commit(&o_full[t]);
-                    issue_qk(t, stK2, nk2);
+                    issue_qk_hook(t, stK2, nk2, pass_turn);
                     tc_commit(&s_full[t]);
                 } else {
                     issue_pv(t, stV, nkv, j > 0);
                     tc_commit(&o_full[t]);
-                    if (more) { issue_qk(t, stK2, nk2); tc_commit(&s_full[t]); }
+                    if (more) {
+                        issue_qk_hook(t, stK2, nk2, pass_turn);
+                        tc_commit(&s_full[t]);
+                    } else {
+                        pass_turn();
+                    }
                 }
-                pass_turn();
                 ++tiles;
                 tc_commit(&kv_empty[stV]);
                 if (more) {
@@ -1165,17 +1191,11 @@ sp_status prefill_impl(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32
     }
     p.n_items = (int32_t)n_items;
     p.inline_words = inl ? (int32_t)words : 0;
-    // Two MMA issuers (one per query tile) save most of an item boundary's
-    // hand-over, where one issuer sits behind its own commits and waits while
-    // the other tile's P is ready, but their block-by-block turn-taking costs
-    // a little on every block: measured +7 % on 8K-token calls (about 12
-    // tiles an item), −3 % on 128K-token calls (about 120).
-    bool two = false;
-    if (!c->geo.fp8 && p.nq == 2 && c->cfg.head_dim == 128) {
-        int64_t tiles_total = 0;
-        for (const Cand& cd : cands) tiles_total += cd.item.w & 0xFFFFF;
-        two = n_items > 0 && tiles_total <= kTwoIssuerTilesPerItem * (int64_t)n_items;
-    }
+    // One MMA issuer per query tile wherever the kernel has that instance:
+    // bf16 K/V, head_dim 128, two query tiles per item (the single issuer
+    // sits behind its own commits and waits while the other tile's P is
+    // ready: 0.67 vs 0.73 of peak on 128K calls, 0.46 vs 0.50 on 8K).
+    const bool two = !c->geo.fp8 && p.nq == 2 && c->cfg.head_dim == 128;
     cudaError_t e = cudaSuccess;
     if (!inl) {
         p.items = c->ws.tiles;
@@ -1203,7 +1223,7 @@ sp_status prefill_impl(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32
     if (c->geo.fp8) {   // FP8 pages (head_dim 128, checked at create)
         SP_PF8(16) SP_PF8(32) SP_PF8(64) SP_PF8(128)
         e = cudaErrorInvalidValue;
-    } else if (two) {   // head_dim 128, two query tiles, short items
+    } else if (two) {   // head_dim 128, two query tiles
         SP_PF2(16) SP_PF2(32) SP_PF2(64) SP_PF2(128)
         e = cudaErrorInvalidValue;
     } else {
