@@ -12,8 +12,11 @@
 //                the page pool), 128-byte swizzled, into a ring of stages.
 //   warp 9       TMEM owner and tcgen05 MMA issuer (one thread): S_t = Q_t K^T
 //                into TMEM, later O_t += P_t V with P_t read from TMEM.
-//   warps 10-11  idle (the producer/MMA warpgroup gives its registers to the
-//                softmax warpgroups with setmaxnreg).
+//   warp 10      second MMA issuer (bf16 K/V, head_dim 128, two query tiles:
+//                warp 9 issues tile 0's MMAs, warp 10 tile 1's); with FP8
+//                history warps 10-11 turn page codes into bf16 stage rows;
+//                otherwise idle (the producer/MMA warpgroup gives its
+//                registers to the softmax warpgroups with setmaxnreg).
 //   warps 0-3    softmax + epilogue of query tile 0; warps 4-7 of tile 1.
 //                Each thread owns one query row: it reads its S row from
 //                TMEM into registers, masks (only on tiles that need it, see
