@@ -731,6 +731,14 @@ def run_ours(args, ws, rank):
                 drec["workload"] = DECODE_WL
                 drec["metric"] = "decode visible-KV GB/s"
                 rec["decode"] = drec
+            # the same batch over FP8 (e4m3) pages, bytes counted as stored
+            fargs = argparse.Namespace(**vars(args))
+            fargs.kv_dtype, fargs.no_cpu_baseline = "fp8", True
+            frec = decode_record(fargs, W.WORKLOADS[DECODE_WL], ws, rank, 64)
+            if rank == 0:
+                frec["workload"] = DECODE_WL
+                frec["metric"] = "decode visible-KV GB/s (FP8 pages)"
+                rec["decode_fp8"] = frec
     if rank != 0:
         return None
     line = {"metric": METRIC, "value": rec.pop("value"), "unit": rec.pop("unit"), "n_gpus": ws,
