@@ -390,6 +390,14 @@ sp_status sp_cache_create(const sp_config* cfg, void* pool, void* meta, void* ws
         delete c;
         return fail(SP_ERR_CUDA, err);
     }
+    if (g.fp8 && cfg->page_size >= 64 &&
+        (!encode_tmap_2d(&c->tm_kpool_half, c->kpool, cfg->head_dim, rows, rowb, box,
+                         cfg->page_size / 2, true, &err, true) ||
+         !encode_tmap_2d(&c->tm_vpool_half, c->vpool, cfg->head_dim, rows, rowb, box,
+                         cfg->page_size / 2, true, &err, true))) {
+        delete c;
+        return fail(SP_ERR_CUDA, err);
+    }
     // Device state: every page free, all units empty, the pool zeroed (slots
     // past a page's valid range are read by the kernels and multiplied by a
     // zero weight, so they must hold finite values).

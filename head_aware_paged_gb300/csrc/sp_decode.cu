@@ -32,14 +32,20 @@ namespace {
 
 constexpr int kConsumerWarps = 4;
 constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 12;
 
 template <int D, int P, bool F8 = false>
 struct DecodeShape {
     static constexpr int kElem = F8 ? 1 : 2;            // bytes per stored element
     static constexpr int kHalves = D * kElem / 128;     // 128-byte column blocks per row
-    static constexpr int kHalfBytes = P * 128;
-    static constexpr int kTileBytes = kHalves * kHalfBytes;   // K (or V) of one page
+    // FP8 pages of 64 or more keys stream as two stages of half a page: twice
+    // the stages in the same memory, so every consumer warp owns three and
+    // has two in flight while it computes one (whole 8 KB-per-K pages gave
+    // six stages, three owner warps, one page in flight each)
+    static constexpr int kSub = (F8 && P >= 64) ? 2 : 1;   // stages per page
+    static constexpr int kStageKeys = P / kSub;
+    static constexpr int kHalfBytes = kStageKeys * 128;
+    static constexpr int kTileBytes = kHalves * kHalfBytes;   // K (or V) of one stage
     static constexpr int kStageBytes = 2 * kTileBytes;
     // FP8 runs two CTAs per SM (twice the warps to hide the per-block
     // latency chain), each with half the stage memory
@@ -67,7 +73,7 @@ k_decode(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtenso
     const int NST = p.nst;
     constexpr int BK = P >= 32 ? 32 : 16;     // keys per warp block
     constexpr int NT = BK / 8;                // S n-tiles per block
-    constexpr int NB = P / BK;                // blocks per page (1, 2 or 4)
+    constexpr int NB = S::kStageKeys / BK;    // blocks per stage (1, 2 or 4)
     static_assert(NB == 1 || NB == 2 || NB == 4, "blocks per page must divide the warp count");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -146,21 +152,35 @@ k_decode(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtenso
                 __syncwarp();
                 if (lane == 0) {
                     const int n = (int)min64(32, x1 - base);
-                    for (int i = 0; i < n; ++i) {
-                        if (pk > 0 && !mbar_wait(&empty[ps], (pk - 1) & 1, abort_flag, p.meta.status))
-                            break;
+                    bool stop = false;
+                    for (int i = 0; i < n && !stop; ++i) {
                         const int4 bi = batch[i];
-                        desc[ps] = make_int4(bi.x, bi.y, bi.w, 0);
-                        mbar_arrive_expect_tx(&full[ps], S::kStageBytes);
-                        uint8_t* kdst = stages + ps * S::kStageBytes;
-                        uint8_t* vdst = kdst + S::kTileBytes;
+                        const int lo = bi.y & 0xFFFF, hi = bi.y >> 16;
                         #pragma unroll
-                        for (int hh = 0; hh < S::kHalves; ++hh) {
-                            tma_load_2d(kdst + hh * S::kHalfBytes, &tmK, &full[ps], hh * 64, bi.z * P);
-                            tma_load_2d(vdst + hh * S::kHalfBytes, &tmV, &full[ps], hh * 64, bi.z * P);
+                        for (int sub = 0; sub < S::kSub; ++sub) {
+                            if (pk > 0 && !mbar_wait(&empty[ps], (pk - 1) & 1, abort_flag, p.meta.status)) {
+                                stop = true;
+                                break;
+                            }
+                            // this stage's slot range, relative to its first key
+                            const int k0 = sub * S::kStageKeys;
+                            const int slo = max(lo - k0, 0), shi = min(hi - k0, S::kStageKeys);
+                            desc[ps] = make_int4(bi.x, slo < shi ? slo | (shi << 16) : 0, bi.w, 0);
+                            if (slo < shi) {
+                                mbar_arrive_expect_tx(&full[ps], S::kStageBytes);
+                                uint8_t* kdst = stages + ps * S::kStageBytes;
+                                uint8_t* vdst = kdst + S::kTileBytes;
+                                #pragma unroll
+                                for (int hh = 0; hh < S::kHalves; ++hh) {
+                                    tma_load_2d(kdst + hh * S::kHalfBytes, &tmK, &full[ps], hh * 64, bi.z * P + k0);
+                                    tma_load_2d(vdst + hh * S::kHalfBytes, &tmV, &full[ps], hh * 64, bi.z * P + k0);
+                                }
+                            } else {
+                                mbar_arrive(&full[ps]);     // no visible slot: nothing to load
+                            }
+                            ++issued;
+                            if (++ps == NST) { ps = 0; ++pk; }
                         }
-                        ++issued;
-                        if (++ps == NST) { ps = 0; ++pk; }
                     }
                 }
                 __syncwarp();
@@ -196,8 +216,9 @@ k_decode(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtenso
     uint32_t qa[D / 16][4];
     float m_run[2], l_run[2];
     float o_acc[D / 8][4];
-    // Consumer warp w < W takes items w, w+W, w+2W, ... of this CTA's stream
-    // (whole pages), so a warp only handles the pages it computes.  W divides
+    // Consumer warp w < W takes stages w, w+W, w+2W, ... of this CTA's stream
+    // (whole pages, or half pages for FP8), so a warp only handles the keys
+    // it computes.  W divides
     // the stage count (the launcher makes NST a multiple of 4, or W = NST
     // below 4 stages), so stage s always belongs to warp s % W and each warp
     // waits for its stages' fills in order -- never for a fill two phases
@@ -206,7 +227,7 @@ k_decode(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtenso
     // only keeps walking, so that every merge barrier still sees all four.
     const int W = p.owners;
     const bool owner = warp < W;
-    int xi = warp;                    // this warp's next item, relative to x0
+    int xi = warp;                    // this warp's next stage fill, relative to x0 * kSub
     int s = warp;                     // its stage (xi % NST)
     uint32_t rounds = 0;              // times that stage has been filled before
     bool dead = false;
@@ -261,7 +282,7 @@ k_decode(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtenso
                 #pragma unroll
                 for (int e = 0; e < 4; ++e) o_acc[nt][e] = 0.f;
         }
-        for (; owner && x0 + xi < ub; xi += W) {
+        for (; owner && x0 * S::kSub + xi < ub * S::kSub; xi += W) {
         if (!dead && !mbar_wait(&full[s], rounds & 1, abort_flag, p.meta.status)) dead = true;
         if (dead) continue;
         const int4 dd = desc[s];
@@ -596,7 +617,10 @@ cudaError_t launch_decode_t(const sp_cache* c, DecodeParams& p, int grid, cudaSt
                                  (int)cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
     }
-    k_decode<D, P, F8><<<grid, kDecodeThreads, smem, s>>>(p, c->tm_kpool, c->tm_vpool);
+    // the tensor maps' box is one stage's keys: a whole page, or half a page
+    const CUtensorMap& tk = Sh::kSub == 2 ? c->tm_kpool_half : c->tm_kpool;
+    const CUtensorMap& tv = Sh::kSub == 2 ? c->tm_vpool_half : c->tm_vpool;
+    k_decode<D, P, F8><<<grid, kDecodeThreads, smem, s>>>(p, tk, tv);
     return cudaGetLastError();
 }
 

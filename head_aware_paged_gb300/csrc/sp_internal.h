@@ -143,6 +143,8 @@ struct sp_cache {
     sp::Workspace ws;
     CUtensorMap tm_kpool;   // [num_pages*P rows][d], box {64 or d, P}, 128B swizzle
     CUtensorMap tm_vpool;
+    CUtensorMap tm_kpool_half;   // FP8 pages of P >= 64: the same with box {d, P / 2}
+    CUtensorMap tm_vpool_half;   // (the decode streams such pages in halves)
     // host mirror (authoritative for lengths, page counts and policies)
     std::vector<sp::UnitPol> h_pol;              // [max_seqs][layers][hkv]
     std::vector<std::vector<int32_t>> h_idx;     // per sequence, CSR by unit
