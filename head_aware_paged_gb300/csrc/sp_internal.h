@@ -161,7 +161,7 @@ struct sp_cache {
     cudaEvent_t stage_ev[kStaging] = {};
     size_t stage_bytes = 0;                       // size of each buffer
     int stage_next = 0;
-    bool prefill_checked[4][4] = {};             // [two issuers ? 3 : FP8 ? 2 : D == 128][log2(P) - 4]: attributes set
+    bool prefill_checked[5][4] = {};             // [speculative ? 4 : two issuers ? 3 : FP8 ? 2 : D == 128][log2(P) - 4]: attributes set
     // Caller's event pair armed by sp_set_launch_events for the next
     // attention call (both null when not armed).
     cudaEvent_t launch_ev[2] = {};

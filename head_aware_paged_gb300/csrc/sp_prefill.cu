@@ -76,6 +76,7 @@ constexpr int kPrefetchTiles = 3;      // K/V tiles brought into L2 ahead of the
 // (1, 2 and 3 measured within 1 % of each other; at the very end, the hand-over
 // left the tensor pipe idle: 0.67 instead of 0.73 of peak on 128K calls).
 constexpr int kTurnEarly = 2;
+constexpr int64_t kSpecTilesPerItem = 32;   // speculative exponentials above this mean item length
 constexpr int64_t kTileCost = 160;     // work-assignment cost of one K/V tile
 constexpr int64_t kItemCost = 480;     // and of one work item's fixed part
 constexpr int kMinPieceTiles = 6;      // key tiles of a piece of a split item, at least
@@ -204,7 +205,7 @@ __device__ __forceinline__ uint32_t lowmask32(int32_t n) {
     return n <= 0 ? 0u : n >= 32 ? 0xFFFFFFFFu : ((1u << n) - 1u);
 }
 
-template <int D, int P, bool F8, bool TWO = false>
+template <int D, int P, bool F8, bool TWO = false, bool SPEC = false>
 __global__ void __launch_bounds__(kPfThreads, 1)
 k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tmQ,
           const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -258,6 +259,12 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
     // by block.  A separate instance: the one-issuer kernel (FP8 history,
     // one query tile, head_dim 64) keeps its code size.
     static_assert(!(TWO && F8), "FP8 history keeps warp 10 for the code conversion");
+    // SPEC (calls of long items, with TWO; the host's choice): each softmax
+    // row takes its exponentials against its running max at once and this
+    // tile's max alongside, redoing them only when the max grew past the lazy
+    // rescale's 2^8 or on an item's first tile.  Measured +4 % on 128K-token
+    // calls (about 130 tiles an item) and -2 % on 8K-token calls (about 12),
+    // whose first tiles take two passes: a separate instance.
     constexpr bool two = TWO;
     constexpr uint32_t nissue = TWO ? 2u : 1u;
 
@@ -751,88 +758,191 @@ k_prefill(const __grid_constant__ PrefillParams p, const __grid_constant__ CUten
                         for (int c = 0; c < 128; ++c)
                             sr[c] = ((vm[c >> 5] >> (c & 31)) & 1u) ? sr[c] : 0xff800000u;
                     }
-                    // row maximum (raw score units; the scale is positive): eight
-                    // running maxima, two new columns each per three-input max
-                    float tmax;
-                    {
+                    if constexpr (!SPEC) {
+                        // row maximum (raw score units; the scale is positive): eight
+                        // running maxima, two new columns each per three-input max
+                        float tmax;
+                        {
+                            float m8[8];
+                            #pragma unroll
+                            for (int a = 0; a < 8; ++a) m8[a] = fmaxf(__uint_as_float(sr[a]), __uint_as_float(sr[8 + a]));
+                            #pragma unroll
+                            for (int e = 16; e < 128; e += 16)
+                                #pragma unroll
+                                for (int a = 0; a < 8; ++a)
+                                    m8[a] = fmax3(m8[a], __uint_as_float(sr[e + a]), __uint_as_float(sr[e + 8 + a]));
+                            tmax = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
+                                         fmaxf(m8[6], m8[7])) * sl2;
+                        }
+                        // online softmax with lazy rescale
+                        float alpha = 1.f;
+                        bool resc = false;
+                        const float m_new = fmaxf(m, tmax);
+                        if (m == -INFINITY) {
+                            m = m_new;
+                        } else if (m_new > m + kRescaleLog2) {
+                            alpha = fast_exp2(m - m_new);
+                            m = m_new;
+                            resc = true;
+                        }
+                        const float mb = m == -INFINITY ? 0.f : m;
+                        // The previous tile's PV must be done before P is overwritten
+                        // and before O is rescaled.  It is: this tile's S arrived
+                        // through a tcgen05.commit issued after that PV, and a commit
+                        // tracks every earlier tcgen05 operation of the issuing
+                        // thread, so no separate wait on o_full is needed here (the
+                        // epilogue still waits for the item's last PV).
+                        if (__any_sync(0xffffffffu, resc)) {
+                            #pragma unroll
+                            for (int ch = 0; ch < D / 16; ++ch) {
+                                uint32_t o[16];
+                                tmem_ld16(tO + ch * 16, o);
+                                #pragma unroll
+                                for (int e2 = 0; e2 < 16; ++e2)
+                                    o[e2] = __float_as_uint(__uint_as_float(o[e2]) * alpha);
+                                tmem_st16(tO + ch * 16, o);
+                            }
+                            tmem_st_wait();
+                        }
+                        // exponentials, row sum, P row -> shared memory in the K-major
+                        // 128-byte-swizzled operand layout (-inf columns give 0).  The
+                        // scale-and-shift and the row sum use packed fp32x2 arithmetic.
+                        uint64_t rsum2[4] = {0ull, 0ull, 0ull, 0ull};
+                        const uint64_t sl2x2 = pack_f32x2(sl2, sl2), nmbx2 = pack_f32x2(-mb, -mb);
+                        // P row as bf16 pairs (column j of the S tile = keys 2j, 2j+1),
+                        // stored to TMEM 32 keys at a time
+                        auto exp_group = [&](int g4) {
+                            uint32_t pk[16];
+                            #pragma unroll
+                            for (int e2 = 0; e2 < 16; ++e2) {
+                                const int c = g4 * 32 + 2 * e2;
+                                const uint64_t x2 = fma_f32x2(pack_u32x2(sr[c], sr[c + 1]), sl2x2, nmbx2);
+                                float x0, x1;
+                                unpack_f32x2(x2, x0, x1);
+                                const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                                rsum2[e2 & 3] = add_f32x2(rsum2[e2 & 3], pack_f32x2(p0, p1));
+                                pk[e2] = pack_bf16(p0, p1);
+                            }
+                            tmem_st16(tS + g4 * 16, pk);
+                        };
+                        // all four groups on every tile (no guards, so the compiler can
+                        // interleave them): past nkeys the row is -inf, P is 0 there,
+                        // and the PV MMA reads only the first nkeys / 2 columns
+                        #pragma unroll
+                        for (int g4 = 0; g4 < 4; ++g4) exp_group(g4);
+                        tmem_st_wait();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&p_full[t]);
+                        // the row sum is not needed by the MMA: fold it after the arrive
+                        float rsum[8];
+                        #pragma unroll
+                        for (int e2 = 0; e2 < 4; ++e2) unpack_f32x2(rsum2[e2], rsum[2 * e2], rsum[2 * e2 + 1]);
+                        const float rs = ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3])) +
+                                         ((rsum[4] + rsum[5]) + (rsum[6] + rsum[7]));
+                        l = l * alpha + rs;
+                    } else {
+                        // Exponentials against the running max m straight away (the
+                        // lazy rescale already lets a score exceed m by up to 2^8),
+                        // with this tile's max taken alongside in the issue slots
+                        // the MUFU-bound exponentials leave free.  Only where a row
+                        // has no max yet (an item's first tiles) or its max grew by
+                        // more than 2^8 is the online state updated, O rescaled and
+                        // the row's exponentials taken again (warp-uniform).
+                        uint64_t rsum2[4] = {0ull, 0ull, 0ull, 0ull};
+                        const uint64_t sl2x2 = pack_f32x2(sl2, sl2);
+                        // P row as bf16 pairs (column j of the S tile = keys 2j, 2j+1),
+                        // stored to TMEM 32 keys at a time
+                        auto exp_group = [&](int g4, uint64_t nmbx2) {
+                            uint32_t pk[16];
+                            #pragma unroll
+                            for (int e2 = 0; e2 < 16; ++e2) {
+                                const int c = g4 * 32 + 2 * e2;
+                                const uint64_t x2 = fma_f32x2(pack_u32x2(sr[c], sr[c + 1]), sl2x2, nmbx2);
+                                float x0, x1;
+                                unpack_f32x2(x2, x0, x1);
+                                const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                                rsum2[e2 & 3] = add_f32x2(rsum2[e2 & 3], pack_f32x2(p0, p1));
+                                pk[e2] = pack_bf16(p0, p1);
+                            }
+                            tmem_st16(tS + g4 * 16, pk);
+                        };
+                        // first pass: exponentials against m (0 while the row has
+                        // none) and the row maximum (raw score units; the scale is
+                        // positive): eight running maxima, two columns per
+                        // three-input max per group of 16
                         float m8[8];
                         #pragma unroll
-                        for (int a = 0; a < 8; ++a) m8[a] = fmaxf(__uint_as_float(sr[a]), __uint_as_float(sr[8 + a]));
-                        #pragma unroll
-                        for (int e = 16; e < 128; e += 16)
+                        for (int a = 0; a < 8; ++a) m8[a] = -INFINITY;
+                        {
+                            const float mb0 = m == -INFINITY ? 0.f : m;
+                            const uint64_t nmbx2 = pack_f32x2(-mb0, -mb0);
                             #pragma unroll
-                            for (int a = 0; a < 8; ++a)
-                                m8[a] = fmax3(m8[a], __uint_as_float(sr[e + a]), __uint_as_float(sr[e + 8 + a]));
-                        tmax = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
-                                     fmaxf(m8[6], m8[7])) * sl2;
-                    }
-                    // online softmax with lazy rescale
-                    float alpha = 1.f;
-                    bool resc = false;
-                    const float m_new = fmaxf(m, tmax);
-                    if (m == -INFINITY) {
-                        m = m_new;
-                    } else if (m_new > m + kRescaleLog2) {
-                        alpha = fast_exp2(m - m_new);
-                        m = m_new;
-                        resc = true;
-                    }
-                    const float mb = m == -INFINITY ? 0.f : m;
-                    // The previous tile's PV must be done before P is overwritten
-                    // and before O is rescaled.  It is: this tile's S arrived
-                    // through a tcgen05.commit issued after that PV, and a commit
-                    // tracks every earlier tcgen05 operation of the issuing
-                    // thread, so no separate wait on o_full is needed here (the
-                    // epilogue still waits for the item's last PV).
-                    if (__any_sync(0xffffffffu, resc)) {
-                        #pragma unroll
-                        for (int ch = 0; ch < D / 16; ++ch) {
-                            uint32_t o[16];
-                            tmem_ld16(tO + ch * 16, o);
-                            #pragma unroll
-                            for (int e2 = 0; e2 < 16; ++e2)
-                                o[e2] = __float_as_uint(__uint_as_float(o[e2]) * alpha);
-                            tmem_st16(tO + ch * 16, o);
+                            for (int g4 = 0; g4 < 4; ++g4) {
+                                #pragma unroll
+                                for (int e = g4 * 32; e < g4 * 32 + 32; e += 16)
+                                    #pragma unroll
+                                    for (int a = 0; a < 8; ++a)
+                                        m8[a] = fmax3(m8[a], __uint_as_float(sr[e + a]), __uint_as_float(sr[e + 8 + a]));
+                                exp_group(g4, nmbx2);
+                            }
                         }
+                        const float tmax = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
+                                                 fmaxf(m8[6], m8[7])) * sl2;
+                        // online softmax with lazy rescale
+                        float alpha = 1.f;
+                        bool resc = false, redo = false;
+                        if (m == -INFINITY) {
+                            m = tmax;                 // stays -inf if nothing visible yet
+                            redo = m != -INFINITY;
+                        } else if (tmax > m + kRescaleLog2) {
+                            alpha = fast_exp2(m - tmax);
+                            m = tmax;
+                            resc = redo = true;
+                        }
+                        if (__any_sync(0xffffffffu, redo)) {
+                            // The previous tile's PV must be done before P is
+                            // overwritten and before O is rescaled.  It is: this
+                            // tile's S arrived through a tcgen05.commit issued after
+                            // that PV, and a commit tracks every earlier tcgen05
+                            // operation of the issuing thread, so no separate wait on
+                            // o_full is needed here (the epilogue still waits for the
+                            // item's last PV).
+                            if (__any_sync(0xffffffffu, resc)) {
+                                #pragma unroll
+                                for (int ch = 0; ch < D / 16; ++ch) {
+                                    uint32_t o[16];
+                                    tmem_ld16(tO + ch * 16, o);
+                                    #pragma unroll
+                                    for (int e2 = 0; e2 < 16; ++e2)
+                                        o[e2] = __float_as_uint(__uint_as_float(o[e2]) * alpha);
+                                    tmem_st16(tO + ch * 16, o);
+                                }
+                                tmem_st_wait();
+                            }
+                            // second pass against the new m (rows that kept theirs
+                            // recompute the same values)
+                            #pragma unroll
+                            for (int e2 = 0; e2 < 4; ++e2) rsum2[e2] = 0ull;
+                            const float mb = m == -INFINITY ? 0.f : m;
+                            const uint64_t nmbx2 = pack_f32x2(-mb, -mb);
+                            #pragma unroll
+                            for (int g4 = 0; g4 < 4; ++g4) exp_group(g4, nmbx2);
+                        }
+                        // past nkeys the row is -inf, P is 0 there, and the PV MMA
+                        // reads only the first nkeys / 2 columns
                         tmem_st_wait();
-                    }
-                    // exponentials, row sum, P row -> shared memory in the K-major
-                    // 128-byte-swizzled operand layout (-inf columns give 0).  The
-                    // scale-and-shift and the row sum use packed fp32x2 arithmetic.
-                    uint64_t rsum2[4] = {0ull, 0ull, 0ull, 0ull};
-                    const uint64_t sl2x2 = pack_f32x2(sl2, sl2), nmbx2 = pack_f32x2(-mb, -mb);
-                    // P row as bf16 pairs (column j of the S tile = keys 2j, 2j+1),
-                    // stored to TMEM 32 keys at a time
-                    auto exp_group = [&](int g4) {
-                        uint32_t pk[16];
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&p_full[t]);
+                        // the row sum is not needed by the MMA: fold it after the arrive
+                        float rsum[8];
                         #pragma unroll
-                        for (int e2 = 0; e2 < 16; ++e2) {
-                            const int c = g4 * 32 + 2 * e2;
-                            const uint64_t x2 = fma_f32x2(pack_u32x2(sr[c], sr[c + 1]), sl2x2, nmbx2);
-                            float x0, x1;
-                            unpack_f32x2(x2, x0, x1);
-                            const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-                            rsum2[e2 & 3] = add_f32x2(rsum2[e2 & 3], pack_f32x2(p0, p1));
-                            pk[e2] = pack_bf16(p0, p1);
-                        }
-                        tmem_st16(tS + g4 * 16, pk);
-                    };
-                    // all four groups on every tile (no guards, so the compiler can
-                    // interleave them): past nkeys the row is -inf, P is 0 there,
-                    // and the PV MMA reads only the first nkeys / 2 columns
-                    #pragma unroll
-                    for (int g4 = 0; g4 < 4; ++g4) exp_group(g4);
-                    tmem_st_wait();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&p_full[t]);
-                    // the row sum is not needed by the MMA: fold it after the arrive
-                    float rsum[8];
-                    #pragma unroll
-                    for (int e2 = 0; e2 < 4; ++e2) unpack_f32x2(rsum2[e2], rsum[2 * e2], rsum[2 * e2 + 1]);
-                    const float rs = ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3])) +
-                                     ((rsum[4] + rsum[5]) + (rsum[6] + rsum[7]));
-                    l = l * alpha + rs;
+                        for (int e2 = 0; e2 < 4; ++e2) unpack_f32x2(rsum2[e2], rsum[2 * e2], rsum[2 * e2 + 1]);
+                        const float rs = ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3])) +
+                                         ((rsum[4] + rsum[5]) + (rsum[6] + rsum[7]));
+                        l = l * alpha + rs;
+                    }
                 }
                 if (!ok) break;
                 // epilogue: O / l -> bf16 rows, LSE
@@ -988,24 +1098,24 @@ static_assert(sizeof(MergeParams) <= 32764, "merge parameters exceed the kernel 
 static_assert(sizeof(PrefillParams) + 5 * sizeof(CUtensorMap) <= 32764,
               "prefill parameters exceed the kernel parameter space");
 
-template <int D, int P, bool F8 = false, bool TWO = false>
+template <int D, int P, bool F8 = false, bool TWO = false, bool SPEC = false>
 cudaError_t launch_prefill_t(sp_cache* c, const PrefillParams& p, int grid,
                              const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                              cudaStream_t s) {
     using Sh = PfShape<D, F8>;
-    bool& checked = c->prefill_checked[TWO ? 3 : F8 ? 2 : D == 128][P == 16 ? 0 : P == 32 ? 1 : P == 64 ? 2 : 3];
+    bool& checked = c->prefill_checked[SPEC ? 4 : TWO ? 3 : F8 ? 2 : D == 128][P == 16 ? 0 : P == 32 ? 1 : P == 64 ? 2 : 3];
     if (!checked) {   // once per cache and kernel instance
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, k_prefill<D, P, F8, TWO>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, k_prefill<D, P, F8, TWO, SPEC>);
         if (e != cudaSuccess) return e;
         // The setmaxnreg split assumes exactly kLaunchRegs registers per thread
         // at launch; anything else could leave an increase waiting forever.
         if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(k_prefill<D, P, F8, TWO>, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmem);
+        e = cudaFuncSetAttribute(k_prefill<D, P, F8, TWO, SPEC>, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmem);
         if (e != cudaSuccess) return e;
         checked = true;
     }
-    k_prefill<D, P, F8, TWO><<<grid, kPfThreads, Sh::kSmem, s>>>(p, tq, tk, tv, c->tm_kpool, c->tm_vpool);
+    k_prefill<D, P, F8, TWO, SPEC><<<grid, kPfThreads, Sh::kSmem, s>>>(p, tq, tk, tv, c->tm_kpool, c->tm_vpool);
     return cudaGetLastError();
 }
 
@@ -1199,6 +1309,14 @@ sp_status prefill_impl(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32
     // sits behind its own commits and waits while the other tile's P is
     // ready: 0.67 vs 0.73 of peak on 128K calls, 0.46 vs 0.50 on 8K).
     const bool two = !c->geo.fp8 && p.nq == 2 && c->cfg.head_dim == 128;
+    // speculative exponentials (SPEC) for calls whose items average more
+    // than kSpecTilesPerItem tiles
+    bool spec = false;
+    if (two) {
+        int64_t tiles_total = 0;
+        for (const Cand& cd : cands) tiles_total += cd.item.w & 0xFFFFF;
+        spec = tiles_total > kSpecTilesPerItem * (int64_t)n_items;
+    }
     cudaError_t e = cudaSuccess;
     if (!inl) {
         p.items = c->ws.tiles;
@@ -1220,7 +1338,8 @@ sp_status prefill_impl(sp_cache* c, int32_t layer, const int32_t* seq_ids, int32
 #define SP_PF(DD, PP) \
     if (D == DD && P == PP) e = launch_prefill_t<DD, PP>(c, p, grid, tq, tk, tv, stream); else
 #define SP_PF2(PP) \
-    if (P == PP) e = launch_prefill_t<128, PP, false, true>(c, p, grid, tq, tk, tv, stream); else
+    if (P == PP) e = spec ? launch_prefill_t<128, PP, false, true, true>(c, p, grid, tq, tk, tv, stream) \
+                          : launch_prefill_t<128, PP, false, true>(c, p, grid, tq, tk, tv, stream); else
 #define SP_PF8(PP) \
     if (D == 128 && P == PP) e = launch_prefill_t<128, PP, true>(c, p, grid, tq, tk, tv, stream); else
     if (c->geo.fp8) {   // FP8 pages (head_dim 128, checked at create)
